@@ -1,0 +1,222 @@
+"""CPU oracle for the VC-Attention hot path -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline /
+reference leg may import this package.  It shares no code with the CUDA
+library (``bit_fp8_attention_means_gb300``) and never imports it; both sides
+receive the same seeded inputs from ``bit_fp8_attention_means_gb300.inputs``.
+
+Every function takes / returns numpy arrays.  bf16 tensors are passed as their
+raw ``uint16`` bit patterns.  Layouts follow the C-ABI of the library:
+Q/K/V ``[B, N, H, d]`` (any strides with unit channel stride), Q8/K8
+``[B, H, Npad, d]``, V8T ``[B, H, d, Npad]``, scales ``[B, H, nblk]`` /
+``[B, H, d]``, means ``[B, H, nblk, d]``.
+
+Parity status of each function is pinned by ``tests/test_oracle_*.py``;
+see the file header of ``vc_oracle.c`` for the passages each step follows.
+"""
+import ctypes
+import math
+import os
+
+import numpy as np
+
+from . import build as _build
+
+BLOCK = 128
+_lib = None
+
+_f32p = np.ctypeslib.ndpointer(np.float32, flags="C_CONTIGUOUS")
+_f64p = np.ctypeslib.ndpointer(np.float64, flags="C_CONTIGUOUS")
+_u8p = np.ctypeslib.ndpointer(np.uint8, flags="C_CONTIGUOUS")
+_u16p = np.ctypeslib.ndpointer(np.uint16, flags="C_CONTIGUOUS")
+_i32p = np.ctypeslib.ndpointer(np.int32, flags="C_CONTIGUOUS")
+_i64 = ctypes.c_int64
+_int = ctypes.c_int
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        _lib = ctypes.CDLL(_build.build())
+        L = _lib
+        L.vco_e4m3_decode.restype = ctypes.c_double
+        L.vco_e4m3_decode.argtypes = [ctypes.c_uint8]
+        L.vco_e4m3_encode.restype = ctypes.c_uint8
+        L.vco_e4m3_encode.argtypes = [ctypes.c_float]
+        L.vco_expcast_C.restype = ctypes.c_float
+        L.vco_expcast_C.argtypes = [ctypes.c_float]
+        L.vco_expcast_code.restype = ctypes.c_uint8
+        L.vco_expcast_code.argtypes = [ctypes.c_float, ctypes.c_float, ctypes.c_float]
+        L.vco_e4m3_encode_arr.argtypes = [_f32p, _i64, _u8p]
+        L.vco_e4m3_decode_arr.argtypes = [_u8p, _i64, _f64p]
+        L.vco_bf16_rne_arr.argtypes = [_f32p, _i64, _u16p]
+        L.vco_expcast_arr.argtypes = [_f32p, _i64, ctypes.c_float, ctypes.c_float, _u8p]
+        L.vco_kmeans.restype = _int
+        L.vco_kmeans.argtypes = [_u16p, _int, _int, _int, _int, _i64, _i64, _i64,
+                                 _int, _int, _int, _f32p, _i32p]
+        L.vco_argsort_labels.restype = _int
+        L.vco_argsort_labels.argtypes = [_i32p, _int, _int, _int, _i32p]
+        L.vco_quantize.restype = _int
+        L.vco_quantize.argtypes = [_u16p, _u16p, _u16p, _int, _int, _int, _int, _i64, _i64, _i64,
+                                   ctypes.c_void_p, _int, _u8p, _f32p, _u8p, _f32p, _u8p, _f32p,
+                                   ctypes.c_void_p]
+        L.vco_attn.restype = _int
+        L.vco_attn.argtypes = [_u8p, _f32p, _u8p, _f32p, _u8p, _f32p, ctypes.c_void_p,
+                               _int, _int, _int, _int, ctypes.c_float, _int, _int,
+                               _i32p, _int, ctypes.c_void_p, _f64p, ctypes.c_void_p]
+        L.vco_attn_ref.restype = _int
+        L.vco_attn_ref.argtypes = [_u16p, _u16p, _u16p, _int, _int, _int, _int, _i64, _i64, _i64,
+                                   ctypes.c_double, _i32p, _int, _f64p]
+        L.vco_num_threads.restype = _int
+    return _lib
+
+
+def num_threads() -> int:
+    return lib().vco_num_threads()
+
+
+def nblk_of(N: int) -> int:
+    return (N + BLOCK - 1) // BLOCK
+
+
+# ---------------------------------------------------------------- codecs
+
+def e4m3_decode(codes) -> np.ndarray:
+    c = np.ascontiguousarray(codes, dtype=np.uint8).ravel()
+    out = np.empty(c.size, np.float64)
+    lib().vco_e4m3_decode_arr(c, c.size, out)
+    return out.reshape(np.shape(codes))
+
+
+def e4m3_encode(x) -> np.ndarray:
+    a = np.ascontiguousarray(x, dtype=np.float32).ravel()
+    out = np.empty(a.size, np.uint8)
+    lib().vco_e4m3_encode_arr(a, a.size, out)
+    return out.reshape(np.shape(x))
+
+
+def bf16_rne(x) -> np.ndarray:
+    a = np.ascontiguousarray(x, dtype=np.float32).ravel()
+    out = np.empty(a.size, np.uint16)
+    lib().vco_bf16_rne_arr(a, a.size, out)
+    return out.reshape(np.shape(x))
+
+
+def bf16_to_f32(bits) -> np.ndarray:
+    b = np.ascontiguousarray(bits, dtype=np.uint16)
+    return (b.astype(np.uint32) << 16).view(np.float32)
+
+
+def kscale_of(softmax_scale: float, d: int) -> np.float32:
+    """fp32(softmax_scale * log2 e); softmax_scale <= 0 means 1/sqrt(d)."""
+    s = np.float32(softmax_scale) if softmax_scale > 0 else np.float32(1.0 / math.sqrt(d))
+    return np.float32(float(s) * (1.0 / math.log(2.0)))
+
+
+def expcast_C(m_new: float) -> np.float32:
+    return np.float32(lib().vco_expcast_C(float(m_new)))
+
+
+def expcast_codes(acc, sigma8: float, C: float) -> np.ndarray:
+    a = np.ascontiguousarray(acc, dtype=np.float32).ravel()
+    out = np.empty(a.size, np.uint8)
+    lib().vco_expcast_arr(a, a.size, float(sigma8), float(C), out)
+    return out.reshape(np.shape(acc))
+
+
+# ---------------------------------------------------------------- path
+
+def _bnhd(X):
+    """uint16 [B,N,H,d] (any layout) -> (contiguous array, strides in elements)."""
+    X = np.ascontiguousarray(X, dtype=np.uint16)
+    B, N, H, d = X.shape
+    return X, (N * H * d, H * d, d)
+
+
+def kmeans(V, k: int, iters: int, centroids=None):
+    """Lloyd k-means per (b,h). Returns (centroids fp32 [B,H,k,d], labels int32 [B,H,N])."""
+    V, (sb, sn, sh) = _bnhd(V)
+    B, N, H, d = V.shape
+    warm = centroids is not None
+    cent = (np.ascontiguousarray(centroids, dtype=np.float32).copy() if warm
+            else np.zeros((B, H, k, d), np.float32))
+    labels = np.zeros((B, H, N), np.int32)
+    rc = lib().vco_kmeans(V, B, H, N, d, sb, sn, sh, k, iters, int(warm), cent, labels)
+    assert rc == 0
+    return cent, labels
+
+
+def argsort_labels(labels, k: int) -> np.ndarray:
+    z = np.ascontiguousarray(labels, dtype=np.int32)
+    B, H, N = z.shape
+    perm = np.zeros_like(z)
+    assert lib().vco_argsort_labels(z, B * H, N, k, perm) == 0
+    return perm
+
+
+def quantize(Q, K, V, perm=None, vsmooth: int = 1):
+    Q, (sb, sn, sh) = _bnhd(Q)
+    K, _ = _bnhd(K)
+    V, _ = _bnhd(V)
+    B, N, H, d = Q.shape
+    nb = nblk_of(N)
+    Npad = nb * BLOCK
+    out = dict(
+        Q8=np.zeros((B, H, Npad, d), np.uint8), sq=np.zeros((B, H, nb), np.float32),
+        K8=np.zeros((B, H, Npad, d), np.uint8), sk=np.zeros((B, H, nb), np.float32),
+        V8T=np.zeros((B, H, d, Npad), np.uint8), sv=np.zeros((B, H, d), np.float32),
+        mu=np.zeros((B, H, nb, d), np.uint16))
+    p = None
+    if perm is not None:
+        perm = np.ascontiguousarray(perm, dtype=np.int32)
+        p = perm.ctypes.data_as(ctypes.c_void_p)
+    rc = lib().vco_quantize(Q, K, V, B, H, N, d, sb, sn, sh, p, int(vsmooth),
+                            out["Q8"], out["sq"], out["K8"], out["sk"], out["V8T"], out["sv"],
+                            out["mu"].ctypes.data_as(ctypes.c_void_p))
+    assert rc == 0
+    return out
+
+
+def attn(qz: dict, N: int, softmax_scale: float = 0.0, expcast: int = 1, vsmooth: int = 1,
+         rows=None, acc_in=None, want_codes: bool = False):
+    """Quantized-path attention for the query rows ``rows`` of every (b,h).
+
+    Returns O fp64 [B,H,nrows,d] (and codes uint8 [B,H,nrows,Npad] if asked).
+    """
+    B, H, Npad, d = qz["Q8"].shape
+    if rows is None:
+        rows = np.arange(N, dtype=np.int32)
+    rows = np.ascontiguousarray(rows, dtype=np.int32)
+    nr = rows.size
+    O = np.zeros((B, H, nr, d), np.float64)
+    P = np.zeros((B, H, nr, Npad), np.uint8) if want_codes else None
+    acc_p = None
+    if acc_in is not None:
+        acc_in = np.ascontiguousarray(acc_in, dtype=np.float32)
+        assert acc_in.shape == (B, H, nr, Npad)
+        acc_p = acc_in.ctypes.data_as(ctypes.c_void_p)
+    mu = np.ascontiguousarray(qz["mu"], dtype=np.uint16)
+    rc = lib().vco_attn(np.ascontiguousarray(qz["Q8"]), np.ascontiguousarray(qz["sq"]),
+                        np.ascontiguousarray(qz["K8"]), np.ascontiguousarray(qz["sk"]),
+                        np.ascontiguousarray(qz["V8T"]), np.ascontiguousarray(qz["sv"]),
+                        mu.ctypes.data_as(ctypes.c_void_p),
+                        B, H, N, d, float(kscale_of(softmax_scale, d)), int(expcast), int(vsmooth),
+                        rows, nr, acc_p, O,
+                        P.ctypes.data_as(ctypes.c_void_p) if P is not None else None)
+    assert rc == 0
+    return (O, P) if want_codes else O
+
+
+def attn_ref(Q, K, V, softmax_scale: float = 0.0, rows=None) -> np.ndarray:
+    """fp64 softmax(Q K^T * scale) V on the bf16 inputs. Returns [B,H,nrows,d]."""
+    Q, (sb, sn, sh) = _bnhd(Q)
+    K, _ = _bnhd(K)
+    V, _ = _bnhd(V)
+    B, N, H, d = Q.shape
+    scale = softmax_scale if softmax_scale > 0 else 1.0 / math.sqrt(d)
+    if rows is None:
+        rows = np.arange(N, dtype=np.int32)
+    rows = np.ascontiguousarray(rows, dtype=np.int32)
+    O = np.zeros((B, H, rows.size, d), np.float64)
+    assert lib().vco_attn_ref(Q, K, V, B, H, N, d, sb, sn, sh, float(scale), rows, rows.size, O) == 0
+    return O

@@ -1,0 +1,489 @@
+/*
+ * vc_oracle.c -- plain, slow CPU oracle for the VC-Attention hot path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path links, loads or
+ * calls this file; it exists so the CUDA library can be checked against an
+ * independent statement of what the method computes.  It shares no code,
+ * header, table or constant generator with the CUDA sources.
+ *
+ * Sources (web pages about the paper "VC-Attention: Value Smoothing and
+ * Softmax Casting for Low-bit Attention"):
+ *   [R]  paper summary on paper.rainbus.top: sections 前置知识 (E4M3 浮点格式,
+ *        在线 softmax) and 方法步骤详情, steps 1-4.
+ *   [D]  study note on dimensionstp.github.io (vc_attention): section 2-1
+ *        (K' = K[pi], V' = V[pi], P'V' = PV), 2-2 (mu_j, R_j), 2-3
+ *        (P_ij V'_j = P_ij R_j + r_ij mu_j^T), 2-4 (ExpCast-FP8).
+ *   [W]  news article on wire.sakhanda.co, sections "V-Smooth" and
+ *        "ExpCast-FP8" (128-token blocks, per-channel E4M3 residual, 79.6%).
+ *
+ * Precision: fp64 wherever the pages leave it open (scores, softmax state,
+ * output, k-means distances and means).  Where a floating-point result
+ * decides an integer code (scales, block means, the ExpCast byte) the
+ * computation is done in fp32, in the order stated next to it, because the
+ * pages fix 8-bit codes and 16-bit means and the code must come out of the
+ * same rounding decisions as the kernel's.
+ *
+ * Build: gcc -O2 -fopenmp -ffp-contract=off -fno-fast-math (see build.py).
+ * -ffp-contract=off keeps every a*b+c below a separately rounded multiply and
+ * add unless fmaf() is written out.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <fenv.h>
+
+#define VCO_BLOCK 128 /* B_v = 128 tokens per hardware block, [R] 复现评估 / [W] */
+
+/* ------------------------------------------------------------------ */
+/* E4M3 (OCP FP8): 1 sign, 4 exponent (bias 7), 3 mantissa bits; no    */
+/* infinities; S.1111.111 is NaN; largest finite magnitude 448. [R]    */
+/* 前置知识 "E4M3 浮点格式".                                            */
+/* ------------------------------------------------------------------ */
+
+double vco_e4m3_decode(uint8_t c) {
+    int s = (c >> 7) & 1;
+    int e = (c >> 3) & 15;
+    int m = c & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) v = (double)m * ldexp(1.0, -9);          /* subnormal: m/8 * 2^(1-7) */
+    else        v = ldexp(1.0 + (double)m / 8.0, e - 7); /* normal */
+    return s ? -v : v;
+}
+
+/* Round-to-nearest, ties to the even code, saturating to +-448 (the
+ * "satfinite" behaviour: anything at or beyond 448 becomes 448). */
+uint8_t vco_e4m3_encode(float xf) {
+    if (isnan(xf)) return 0x7F;
+    uint8_t sign = signbit(xf) ? 0x80 : 0x00;
+    double a = fabs((double)xf);
+    if (a == 0.0) return sign;
+    if (a >= 448.0) return sign | 0x7E;
+    int e2;
+    frexp(a, &e2);           /* a = f * 2^e2, f in [0.5, 1) */
+    int E = e2 - 1;          /* floor(log2 a) */
+    if (E < -6) {
+        /* subnormal grid: multiples of 2^-9; rounding up to 8 gives the
+         * smallest normal 0x08 = 2^-6, which is the right neighbour. */
+        double q = a * 512.0;                 /* exact */
+        double mq = nearbyint(q);             /* RNE (default mode) */
+        return sign | (uint8_t)mq;
+    }
+    double q = a / ldexp(1.0, E - 3);         /* exact, in [8, 16) */
+    double mq = nearbyint(q);                 /* in [8, 16]; mantissa parity = mq parity */
+    int EE = E + 7;
+    if (mq == 16.0) { mq = 8.0; EE += 1; }
+    int code = (EE << 3) | ((int)mq - 8);
+    if (code > 0x7E) code = 0x7E;
+    return sign | (uint8_t)code;
+}
+
+/* bfloat16: the upper 16 bits of an fp32, rounded to nearest even. */
+uint16_t vco_bf16_rne(float f) {
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    if ((u & 0x7FFFFFFFu) > 0x7F800000u) return (uint16_t)((u >> 16) | 0x0040u); /* quiet NaN */
+    uint32_t keep = u >> 16, rest = u & 0xFFFFu;
+    if (rest > 0x8000u || (rest == 0x8000u && (keep & 1u))) keep += 1u;
+    return (uint16_t)keep;
+}
+
+float vco_bf16_to_f32(uint16_t h) {
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+/* ------------------------------------------------------------------ */
+/* ExpCast-FP8.  [R] 方法步骤详情 step 4 and 前置知识 "E4M3 浮点格式":   */
+/* the E4M3 byte read as an integer is 8*log2(v) + 56 + eps(m), so a    */
+/* probability 2^(u+8) (u <= 0 in log2 units, factor 2^8 puts the row   */
+/* maximum at v = 256 = byte 120) is written directly as               */
+/*     c = clip(Round(8*(u + 8) + 56 + beta), 0, 120),  beta = -0.35.   */
+/* With u = sigma*acc - m' this is one FMA: t = acc*(8 sigma) + C with  */
+/* C = 119.65 - 8 m'.  Round is round-half-even; the byte is then read  */
+/* as an E4M3 code (bytes 1..7 are the subnormal underflow tail).       */
+/* ------------------------------------------------------------------ */
+
+#define VCO_BETA_PLUS_120 119.65f /* 120 + beta, beta = -0.35 ([R] step 4, 复现评估) */
+
+float vco_expcast_C(float m_new) { return fmaf(-8.0f, m_new, VCO_BETA_PLUS_120); }
+
+uint8_t vco_expcast_code(float acc, float sigma8, float C) {
+    float t = fmaf(acc, sigma8, C);
+    float r = nearbyintf(t);                  /* RNE */
+    if (!(r > 0.0f)) return 0;                /* negatives, -0, -inf, NaN */
+    if (r > 120.0f) return 120;
+    return (uint8_t)r;
+}
+
+/* ------------------------------------------------------------------ */
+/* Vectorised helpers for the Python side.                             */
+/* ------------------------------------------------------------------ */
+
+void vco_e4m3_encode_arr(const float* x, int64_t n, uint8_t* out) {
+    #pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i) out[i] = vco_e4m3_encode(x[i]);
+}
+
+void vco_e4m3_decode_arr(const uint8_t* c, int64_t n, double* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = vco_e4m3_decode(c[i]);
+}
+
+void vco_bf16_rne_arr(const float* x, int64_t n, uint16_t* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = vco_bf16_rne(x[i]);
+}
+
+void vco_expcast_arr(const float* acc, int64_t n, float sigma8, float C, uint8_t* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = vco_expcast_code(acc[i], sigma8, C);
+}
+
+/* ------------------------------------------------------------------ */
+/* Step 1, grouping: online (inference-time) k-means on the value       */
+/* tokens of each (batch, head), then pi = argsort(z).  [R] step 1,     */
+/* [D] 2-1.  Lloyd iterations; each iteration assigns every token to    */
+/* its nearest centroid (squared Euclidean distance, ties to the lowest */
+/* index) and then moves each centroid to the mean of its tokens; an    */
+/* empty cluster keeps its centroid.  Cold start: centroid i is token   */
+/* floor(i*N/k).  Warm start: the caller's centroids.                   */
+/* ------------------------------------------------------------------ */
+
+static const uint16_t* tok(const uint16_t* X, int64_t s_b, int64_t s_n, int64_t s_h,
+                           int b, int h, int n) {
+    return X + (int64_t)b * s_b + (int64_t)n * s_n + (int64_t)h * s_h;
+}
+
+int vco_kmeans(const uint16_t* V, int B, int H, int N, int d,
+               int64_t s_b, int64_t s_n, int64_t s_h,
+               int k, int iters, int warm, float* cent /* [B,H,k,d] */,
+               int32_t* labels /* [B,H,N] */) {
+    if (k < 1 || iters < 1 || N < 1) return 1;
+    #pragma omp parallel for schedule(dynamic)
+    for (int bh = 0; bh < B * H; ++bh) {
+        int b = bh / H, h = bh % H;
+        float* C = cent + (int64_t)bh * k * d;
+        int32_t* z = labels + (int64_t)bh * N;
+        double* vrow = (double*)malloc(sizeof(double) * d);
+        double* sum = (double*)malloc(sizeof(double) * (size_t)k * d);
+        int64_t* cnt = (int64_t*)malloc(sizeof(int64_t) * k);
+        if (!warm) {
+            for (int i = 0; i < k; ++i) {
+                int src = (int)(((int64_t)i * N) / k);
+                const uint16_t* v = tok(V, s_b, s_n, s_h, b, h, src);
+                for (int c = 0; c < d; ++c) C[(int64_t)i * d + c] = vco_bf16_to_f32(v[c]);
+            }
+        }
+        for (int it = 0; it < iters; ++it) {
+            /* assignment */
+            for (int n = 0; n < N; ++n) {
+                const uint16_t* v = tok(V, s_b, s_n, s_h, b, h, n);
+                for (int c = 0; c < d; ++c) vrow[c] = (double)vco_bf16_to_f32(v[c]);
+                double best = INFINITY;
+                int arg = 0;
+                for (int i = 0; i < k; ++i) {
+                    double dist = 0.0;
+                    for (int c = 0; c < d; ++c) {
+                        double df = vrow[c] - (double)C[(int64_t)i * d + c];
+                        dist += df * df;
+                    }
+                    if (dist < best) { best = dist; arg = i; }
+                }
+                z[n] = arg;
+            }
+            /* update: mean of the members */
+            memset(sum, 0, sizeof(double) * (size_t)k * d);
+            memset(cnt, 0, sizeof(int64_t) * k);
+            for (int n = 0; n < N; ++n) {
+                const uint16_t* v = tok(V, s_b, s_n, s_h, b, h, n);
+                cnt[z[n]] += 1;
+                for (int c = 0; c < d; ++c) sum[(int64_t)z[n] * d + c] += (double)vco_bf16_to_f32(v[c]);
+            }
+            for (int i = 0; i < k; ++i) {
+                if (cnt[i] == 0) continue;
+                for (int c = 0; c < d; ++c)
+                    C[(int64_t)i * d + c] = (float)(sum[(int64_t)i * d + c] / (double)cnt[i]);
+            }
+        }
+        free(vrow); free(sum); free(cnt);
+    }
+    return 0;
+}
+
+/* pi = argsort(z), stable: ascending label, equal labels keep token order
+ * (the pages give no tie rule; a stable order is the plainest reading). */
+int vco_argsort_labels(const int32_t* labels, int BH, int N, int k, int32_t* perm) {
+    #pragma omp parallel for schedule(dynamic)
+    for (int bh = 0; bh < BH; ++bh) {
+        const int32_t* z = labels + (int64_t)bh * N;
+        int32_t* p = perm + (int64_t)bh * N;
+        int pos = 0;
+        for (int lab = 0; lab < k; ++lab)
+            for (int n = 0; n < N; ++n)
+                if (z[n] == lab) p[pos++] = n;
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* Step 2, block quantization.                                          */
+/*  Q and K' = K[pi]: one fp32 scale per 128-token block ([R] 前置知识  */
+/*  "低比特量化与离群值": every hardware block shares one scale s_X):   */
+/*      amax = max |x| over the block's valid tokens and all channels,  */
+/*      s = amax / 448, inv = 448 / amax (0 if amax = 0),               */
+/*      code = E4M3_RNE_sat(x * inv)   (fp32 multiply).                 */
+/*  V' = V[pi] ([D] 2-2, [R] step 2): mu_j = (1/B_v) V'_j^T 1 kept in    */
+/*  16 bits (bf16), R_j = V'_j - 1 mu_j^T, residual quantized to E4M3   */
+/*  with one scale per channel over the whole sequence of the head.    */
+/*      sum  = fp32 sum over the block's valid tokens in token order,   */
+/*      mu   = bf16_RNE(sum / count)   (fp32 division),                 */
+/*      R    = fp32(V' - float(mu)),                                    */
+/*      s_v  = max_t |R[t,c]| / 448,  code = E4M3_RNE_sat(R * 448/amax).*/
+/*  With vsmooth = 0, mu = 0 and V' itself is quantized per channel.    */
+/*  Padding tokens (t >= N, up to the next multiple of 128) are code 0. */
+/*  Layouts: X8 [B,H,Npad,d]; s_x [B,H,nblk]; V8T [B,H,d,Npad];         */
+/*  s_v [B,H,d]; mu [B,H,nblk,d] (bf16 bits).                           */
+/* ------------------------------------------------------------------ */
+
+static void quant_rows_blockscale(const uint16_t* X, int64_t s_b, int64_t s_n, int64_t s_h,
+                                  int b, int h, int N, int d, const int32_t* perm_bh,
+                                  uint8_t* X8, float* sx) {
+    int nblk = (N + VCO_BLOCK - 1) / VCO_BLOCK;
+    for (int j = 0; j < nblk; ++j) {
+        int t0 = j * VCO_BLOCK;
+        float amax = 0.0f;
+        for (int t = t0; t < t0 + VCO_BLOCK && t < N; ++t) {
+            int src = perm_bh ? perm_bh[t] : t;
+            const uint16_t* x = tok(X, s_b, s_n, s_h, b, h, src);
+            for (int c = 0; c < d; ++c) {
+                float a = fabsf(vco_bf16_to_f32(x[c]));
+                if (a > amax) amax = a;
+            }
+        }
+        float s = amax / 448.0f;
+        float inv = (amax > 0.0f) ? 448.0f / amax : 0.0f;
+        sx[j] = s;
+        for (int t = t0; t < t0 + VCO_BLOCK; ++t) {
+            uint8_t* out = X8 + (int64_t)t * d;
+            if (t >= N) { memset(out, 0, (size_t)d); continue; }
+            int src = perm_bh ? perm_bh[t] : t;
+            const uint16_t* x = tok(X, s_b, s_n, s_h, b, h, src);
+            for (int c = 0; c < d; ++c) out[c] = vco_e4m3_encode(vco_bf16_to_f32(x[c]) * inv);
+        }
+    }
+}
+
+int vco_quantize(const uint16_t* Q, const uint16_t* K, const uint16_t* V,
+                 int B, int H, int N, int d, int64_t s_b, int64_t s_n, int64_t s_h,
+                 const int32_t* perm, int vsmooth,
+                 uint8_t* Q8, float* sq, uint8_t* K8, float* sk,
+                 uint8_t* V8T, float* sv, uint16_t* mu) {
+    if (N < 1 || d < 1) return 1;
+    int nblk = (N + VCO_BLOCK - 1) / VCO_BLOCK;
+    int64_t Npad = (int64_t)nblk * VCO_BLOCK;
+    #pragma omp parallel for schedule(dynamic)
+    for (int bh = 0; bh < B * H; ++bh) {
+        int b = bh / H, h = bh % H;
+        const int32_t* p = perm ? perm + (int64_t)bh * N : NULL;
+        quant_rows_blockscale(Q, s_b, s_n, s_h, b, h, N, d, NULL,
+                              Q8 + (int64_t)bh * Npad * d, sq + (int64_t)bh * nblk);
+        quant_rows_blockscale(K, s_b, s_n, s_h, b, h, N, d, p,
+                              K8 + (int64_t)bh * Npad * d, sk + (int64_t)bh * nblk);
+        /* V': block means, residuals, per-channel scale */
+        float* R = (float*)malloc(sizeof(float) * (size_t)N * d);
+        for (int j = 0; j < nblk; ++j) {
+            int t0 = j * VCO_BLOCK;
+            int cnt = (N - t0 < VCO_BLOCK) ? (N - t0) : VCO_BLOCK;
+            for (int c = 0; c < d; ++c) {
+                float m = 0.0f;
+                if (vsmooth) {
+                    float sum = 0.0f;
+                    for (int t = t0; t < t0 + cnt; ++t) {
+                        int src = p ? p[t] : t;
+                        sum = sum + vco_bf16_to_f32(tok(V, s_b, s_n, s_h, b, h, src)[c]);
+                    }
+                    uint16_t mb = vco_bf16_rne(sum / (float)cnt);
+                    mu[((int64_t)bh * nblk + j) * d + c] = mb;
+                    m = vco_bf16_to_f32(mb);
+                }
+                for (int t = t0; t < t0 + cnt; ++t) {
+                    int src = p ? p[t] : t;
+                    R[(int64_t)t * d + c] = vco_bf16_to_f32(tok(V, s_b, s_n, s_h, b, h, src)[c]) - m;
+                }
+            }
+        }
+        for (int c = 0; c < d; ++c) {
+            float amax = 0.0f;
+            for (int t = 0; t < N; ++t) {
+                float a = fabsf(R[(int64_t)t * d + c]);
+                if (a > amax) amax = a;
+            }
+            float inv = (amax > 0.0f) ? 448.0f / amax : 0.0f;
+            sv[(int64_t)bh * d + c] = amax / 448.0f;
+            uint8_t* row = V8T + ((int64_t)bh * d + c) * Npad;
+            for (int64_t t = 0; t < Npad; ++t)
+                row[t] = (t < N) ? vco_e4m3_encode(R[t * d + c] * inv) : 0;
+        }
+        free(R);
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* Steps 3-4, attention with the online softmax ([R] 前置知识 "在线     */
+/* softmax": running max m_i, normaliser l_i, numerator A_i, rescale    */
+/* alpha_i = exp(m_i - m'_i); [R] step 3 and [D] 2-3: mean restore      */
+/*     A_i <- alpha_i A_i + P_q,ij R_q,j + r_ij mu_j^T,  r_ij = P_ij 1; */
+/* [R] step 4: ExpCast bytes).                                          */
+/* Keys are visited in 128-token tiles in stored (permuted) order; the  */
+/* running max m' after tile j is the max of the scaled scores seen so  */
+/* far, so every u = sigma*acc - m' <= 0.  Scores in log2 units:        */
+/*     acc   = sum_c q8*k8 (exact in fp64, rounded once to fp32),       */
+/*     sigma = fp32(fp32(sq_i * sk_j) * kscale),                        */
+/*     kscale = fp32(softmax_scale * log2 e)  (the caller passes it),   */
+/*     m'    = max(m, fp32(sigma * max_k acc)).                         */
+/* P entries are the decoded codes (they carry the 2^8 factor, which    */
+/* cancels in A/l).  expcast = 0 is the exp-then-cast path:             */
+/*     code = E4M3_RNE_sat(fp32(exp2(fmaf(acc, sigma, fp32(8 - m'))))). */
+/* Output row: O = A / l (fp64).  acc_in, when given, replaces the      */
+/* computed scores (the ExpCast byte check feeds both sides the same    */
+/* fp32 scores); P_out, when given, receives the codes.                 */
+/* ------------------------------------------------------------------ */
+
+int vco_attn(const uint8_t* Q8, const float* sq, const uint8_t* K8, const float* sk,
+             const uint8_t* V8T, const float* sv, const uint16_t* mu,
+             int B, int H, int N, int d, float kscale, int expcast, int vsmooth,
+             const int32_t* rows, int nrows, const float* acc_in,
+             double* O /* [B,H,nrows,d] */, uint8_t* P_out /* [B,H,nrows,Npad] or NULL */) {
+    if (N < 1 || d < 1) return 1;
+    int nblk = (N + VCO_BLOCK - 1) / VCO_BLOCK;
+    int64_t Npad = (int64_t)nblk * VCO_BLOCK;
+    double dec[256];
+    for (int i = 0; i < 256; ++i) dec[i] = vco_e4m3_decode((uint8_t)i);
+    for (int bh = 0; bh < B * H; ++bh) {
+        /* decoded residual values in [token][channel] order */
+        double* Vd = (double*)malloc(sizeof(double) * (size_t)Npad * d);
+        for (int c = 0; c < d; ++c)
+            for (int64_t t = 0; t < Npad; ++t)
+                Vd[t * d + c] = dec[V8T[((int64_t)bh * d + c) * Npad + t]] * (double)sv[(int64_t)bh * d + c];
+        #pragma omp parallel for schedule(dynamic)
+        for (int ri = 0; ri < nrows; ++ri) {
+            int i = rows[ri];
+            const uint8_t* q = Q8 + ((int64_t)bh * Npad + i) * d;
+            float sqi = sq[(int64_t)bh * nblk + i / VCO_BLOCK];
+            double* A = O + ((int64_t)bh * nrows + ri) * d;
+            double qd[256];
+            for (int c = 0; c < d; ++c) { qd[c] = dec[q[c]]; A[c] = 0.0; }
+            float accv[VCO_BLOCK];
+            uint8_t code[VCO_BLOCK];
+            float m = -INFINITY;
+            double l = 0.0;
+            for (int j = 0; j < nblk; ++j) {
+                int t0 = j * VCO_BLOCK;
+                int cnt = (N - t0 < VCO_BLOCK) ? (N - t0) : VCO_BLOCK;
+                float sigma = (sqi * sk[(int64_t)bh * nblk + j]) * kscale;
+                float mx = -INFINITY;
+                for (int kk = 0; kk < cnt; ++kk) {
+                    if (acc_in) {
+                        accv[kk] = acc_in[((int64_t)bh * nrows + ri) * Npad + t0 + kk];
+                    } else {
+                        const uint8_t* kr = K8 + ((int64_t)bh * Npad + t0 + kk) * d;
+                        double s = 0.0;
+                        for (int c = 0; c < d; ++c) s += qd[c] * dec[kr[c]];
+                        accv[kk] = (float)s;
+                    }
+                    if (accv[kk] > mx) mx = accv[kk];
+                }
+                float mnew = fmaxf(m, sigma * mx);
+                double alpha = (m == -INFINITY) ? 0.0 : exp2((double)m - (double)mnew);
+                double r = 0.0;
+                if (expcast) {
+                    float C = vco_expcast_C(mnew);
+                    float sig8 = 8.0f * sigma;
+                    for (int kk = 0; kk < cnt; ++kk) code[kk] = vco_expcast_code(accv[kk], sig8, C);
+                } else {
+                    float off = 8.0f - mnew;
+                    for (int kk = 0; kk < cnt; ++kk) {
+                        float x = fmaf(accv[kk], sigma, off);
+                        code[kk] = vco_e4m3_encode((float)exp2((double)x));
+                    }
+                }
+                for (int kk = cnt; kk < VCO_BLOCK; ++kk) code[kk] = 0;
+                for (int kk = 0; kk < cnt; ++kk) r += dec[code[kk]];
+                l = alpha * l + r;
+                for (int c = 0; c < d; ++c) A[c] *= alpha;
+                for (int kk = 0; kk < cnt; ++kk) {
+                    double p = dec[code[kk]];
+                    if (p == 0.0) continue;
+                    const double* vr = Vd + (int64_t)(t0 + kk) * d;
+                    for (int c = 0; c < d; ++c) A[c] += p * vr[c];
+                }
+                if (vsmooth) {
+                    const uint16_t* mj = mu + ((int64_t)bh * nblk + j) * d;
+                    for (int c = 0; c < d; ++c) A[c] += r * (double)vco_bf16_to_f32(mj[c]);
+                }
+                if (P_out) memcpy(P_out + ((int64_t)bh * nrows + ri) * Npad + t0, code, VCO_BLOCK);
+                m = mnew;
+            }
+            for (int c = 0; c < d; ++c) A[c] /= l;
+        }
+        free(Vd);
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* Fidelity reference: O = softmax(Q K^T * scale) V in fp64 on the       */
+/* unquantized bf16 inputs ([D] 1-1: O = PV, P = softmax(QK^T/sqrt d)).  */
+/* ------------------------------------------------------------------ */
+
+int vco_attn_ref(const uint16_t* Q, const uint16_t* K, const uint16_t* V,
+                 int B, int H, int N, int d, int64_t s_b, int64_t s_n, int64_t s_h,
+                 double scale, const int32_t* rows, int nrows, double* O) {
+    for (int bh = 0; bh < B * H; ++bh) {
+        int b = bh / H, h = bh % H;
+        double* Kd = (double*)malloc(sizeof(double) * (size_t)N * d);
+        double* Vd = (double*)malloc(sizeof(double) * (size_t)N * d);
+        for (int n = 0; n < N; ++n)
+            for (int c = 0; c < d; ++c) {
+                Kd[(int64_t)n * d + c] = vco_bf16_to_f32(tok(K, s_b, s_n, s_h, b, h, n)[c]);
+                Vd[(int64_t)n * d + c] = vco_bf16_to_f32(tok(V, s_b, s_n, s_h, b, h, n)[c]);
+            }
+        #pragma omp parallel for schedule(dynamic)
+        for (int ri = 0; ri < nrows; ++ri) {
+            int i = rows[ri];
+            double qd[256];
+            for (int c = 0; c < d; ++c) qd[c] = vco_bf16_to_f32(tok(Q, s_b, s_n, s_h, b, h, i)[c]);
+            double* s = (double*)malloc(sizeof(double) * N);
+            double mx = -INFINITY;
+            for (int n = 0; n < N; ++n) {
+                double acc = 0.0;
+                for (int c = 0; c < d; ++c) acc += qd[c] * Kd[(int64_t)n * d + c];
+                s[n] = acc * scale;
+                if (s[n] > mx) mx = s[n];
+            }
+            double l = 0.0;
+            double* o = O + ((int64_t)bh * nrows + ri) * d;
+            for (int c = 0; c < d; ++c) o[c] = 0.0;
+            for (int n = 0; n < N; ++n) {
+                double p = exp(s[n] - mx);
+                l += p;
+                for (int c = 0; c < d; ++c) o[c] += p * Vd[(int64_t)n * d + c];
+            }
+            for (int c = 0; c < d; ++c) o[c] /= l;
+            free(s);
+        }
+        free(Kd); free(Vd);
+    }
+    return 0;
+}
+
+int vco_num_threads(void) {
+#ifdef _OPENMP
+    extern int omp_get_max_threads(void);
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

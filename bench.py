@@ -1,0 +1,441 @@
+"""Benchmark of the VC-Attention hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--mode step|schedule|sweep]
+
+Default (mode=step): the Wan2.2-shaped workload (B=1, H=40, N=75,600, d=128,
+k=256).  One step = one grouping denoising step of the whole path: warm-started
+k-means (1 Lloyd iteration) + stable counting sort, the fused quantizer, and
+the FP8 attention with ExpCast and the V-Smooth mean restore.  The headline
+metric is FP8 attention TFLOPS, 4 B H N^2 d per step divided by the step time
+(the whole step is timed, so grouping and quantization count against it).
+Inputs (2.3 GB) are larger than the 129 MB L2, so no flush is needed between
+steps.  Under torchrun every rank runs the full workload on its own GPU (weak
+scaling, no collective on the data path); the time is the max over ranks.
+
+--impl reference times the CPU oracle (the only other implementation of the
+method that exists) on a bounded sample of the same workload.
+"""
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "FP8 attention TFLOPS at N=75,600 H=40 d=128; % of GB300 dense FP8 peak"
+FP8_PER_BF16 = 2.0   # nominal dense fp8 / bf16 tensor rate (4.5 / 2.25 PFLOP/s)
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--mode", default="step", choices=["step", "schedule", "sweep"])
+    ap.add_argument("--expcast", type=int, default=1)
+    ap.add_argument("--vsmooth", type=int, default=1)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    return ap.parse_args()
+
+
+class ClockSampler:
+    """nvidia-smi sampled every 200 ms while the timed region runs."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.QUERY,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in getattr(self, "lines", []):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": 0}
+        loaded = [s for s in sm if mx is None or s >= 0.3 * mx] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def dist_setup(args):
+    """Returns (rank, world, local_rank, pg_ready)."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+        return rank, world, local, True
+    return rank, world, local, False
+
+
+def max_over_ranks(x, pg_ready):
+    """Max of a float over ranks (identity without a process group)."""
+    if not pg_ready:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if torch.cuda.is_available() else torch.device("cpu")
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(pg_ready):
+    if pg_ready:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def attn_flops(B, H, N, d):
+    return 4.0 * B * H * N * N * d
+
+
+def kernel_source_hash():
+    import hashlib
+    h = hashlib.sha256()
+    for name in ("vc_attn.cu", "vc_device.cuh"):
+        with open(os.path.join(ROOT, "bit_fp8_attention_means_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on this source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(kernel)
+    if not e or e.get("source_hash") != kernel_source_hash():
+        return None
+    return e.get("bytes_per_launch_full_size")
+
+
+def cpu_baseline_sample(Qc, Kc, Vc, perm_h0, N, d, target_s=15.0):
+    """The oracle, as it stands, on a bounded sample: attention rows of head 0."""
+    import numpy as np
+
+    import oracle
+    from bit_fp8_attention_means_gb300 import inputs
+    u16 = inputs.to_u16
+    qz = oracle.quantize(u16(Qc), u16(Kc), u16(Vc), perm_h0, 1)
+    rng = np.random.default_rng(0)
+    probe = np.sort(rng.choice(N, 16, replace=False)).astype(np.int32)
+    t0 = time.perf_counter()
+    oracle.attn(qz, N, rows=probe)
+    per_row = (time.perf_counter() - t0) / probe.size
+    R = int(max(16, min(8192, target_s / max(per_row, 1e-6))))
+    rows = np.sort(rng.choice(N, R, replace=False)).astype(np.int32)
+    t0 = time.perf_counter()
+    oracle.attn(qz, N, rows=rows)
+    dt = time.perf_counter() - t0
+    flops = 4.0 * R * N * d
+    return {"value": flops / dt / 1e12, "unit": "TFLOPS", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": "oracle attention (ExpCast, V-Smooth) on %d random query rows of head 0 against all "
+                      "%d keys, inputs quantized by the oracle from the same bf16 tensors; %.1f s" % (R, N, dt)}
+
+
+def run_ours(args):
+    import torch
+
+    from bit_fp8_attention_means_gb300 import inputs, schedule, vc
+    rank, world, local, pg = dist_setup(args)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = inputs.WORKLOADS["wan"]
+    B, H, N, d, k = w.B, w.H, w.N, w.d, w.k
+    warm_iters = 1
+    ec, vs = args.expcast, args.vsmooth
+    Q, K, V = inputs.make_qkv(w, dev, seed=w.seed + rank)
+    state = schedule.GroupingState()
+    qz, O = schedule.run_step(state, Q, K, V, 0, 1, k, w.iters, warm_iters, expcast=ec, vsmooth=vs,
+                              force_cluster=True)
+    stream = torch.cuda.current_stream()
+
+    def step(times):
+        nonlocal qz, O
+        qz, O = schedule.run_step(state, Q, K, V, 1, 1, k, w.iters, warm_iters, qz=qz, O=O, expcast=ec,
+                                  vsmooth=vs, times=times, force_cluster=True)
+
+    for _ in range(args.warmup):
+        step(None)
+    torch.cuda.synchronize()
+    barrier(pg)
+    times = schedule.StepTimes()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        e0.record(stream)
+        for _ in range(args.steps):
+            step(times)
+        e1.record(stream)
+        torch.cuda.synchronize()
+    barrier(pg)
+    ms = e0.elapsed_time(e1) / args.steps
+    ms_max = max_over_ranks(ms, pg)
+    schedule.collect(times)
+    attn_ms = statistics.mean(times.attn_ms)
+    flops = attn_flops(B, H, N, d)
+    peaks = measured_peaks()
+    fp8_peak = peaks["bf16_tflops_sustained"] * FP8_PER_BF16
+    achieved = flops / (attn_ms * 1e-3) / 1e12
+    launches_per_step = (6 * warm_iters if vs else 0) + 3 + 1
+    result = {
+        "metric": METRIC,
+        "value": world * flops / (ms_max * 1e-3) / 1e12,
+        "unit": "TFLOPS",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3",
+        "data": "synthetic: seeded Wan2.2-shaped Q/K/V (Q,K ~ N(0,1) + per-channel bias N(0,2); V a 256-centroid "
+                "mixture with 1% outlier tokens x20)",
+        "config": {"workload": "wan2.2-shaped B=%d H=%d N=%d d=%d, k=%d" % (B, H, N, d, k),
+                   "step": "grouping step: k-means (warm, %d iteration) + stable sort + fused quantizer + FP8 "
+                           "attention (expcast=%d, vsmooth=%d)" % (warm_iters, ec, vs),
+                   "expcast": ec, "vsmooth": vs, "l2": "inputs 2.3 GB > 129 MB L2; no flush needed",
+                   "parallelism": "replicas x%d (weak scaling, no collective on the data path)" % world},
+        "attn_tflops": achieved,
+        "pct_fp8_peak": 100.0 * achieved / fp8_peak,
+        "pct_fp8_nominal": 100.0 * achieved / 4500.0,
+        "breakdown_ms": {"cluster": statistics.mean(times.cluster_ms), "quantize": statistics.mean(times.quantize_ms),
+                         "attn": attn_ms},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
+                     "frac": achieved / fp8_peak, "traffic": ncu_traffic("attn_fwd_kernel"),
+                     "kernel": "attn_fwd_kernel<128,expcast,vsmooth>",
+                     "peak_source": "%s bf16 sustained %.1f TFLOP/s x %.0f (nominal fp8/bf16 ratio)"
+                                    % (peaks["source"], peaks["bf16_tflops_sustained"], FP8_PER_BF16)},
+        "clocks": clk.summary(),
+        "gpu_launches": launches_per_step * args.steps,
+    }
+    if not args.no_e2e:
+        result["e2e"] = e2e_run(args, Q, K, V, state, step_fn=lambda: step(None), O_ref=lambda: O)
+    if rank == 0 and world == 1 and not args.no_cpu:
+        Qc, Kc, Vc = (t[:, :, :1].cpu() for t in (Q, K, V))
+        result["cpu_baseline"] = cpu_baseline_sample(Qc, Kc, Vc, state.perm[:, :1].cpu().numpy(), N, d)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if pg:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def e2e_run(args, Q, K, V, state, step_fn, O_ref):
+    """Same metric through the public API with host buffers: pinned H2D of Q/K/V and D2H of O every step."""
+    import torch
+    w_steps = max(1, min(args.steps, 3))
+    hQ, hK, hV = (t.cpu().pin_memory() for t in (Q, K, V))
+    hO = torch.empty(Q.shape, dtype=Q.dtype).pin_memory()
+    stream = torch.cuda.current_stream()
+
+    def one():
+        Q.copy_(hQ, non_blocking=True)
+        K.copy_(hK, non_blocking=True)
+        V.copy_(hV, non_blocking=True)
+        step_fn()
+        hO.copy_(O_ref(), non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(w_steps):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / w_steps
+    B, N, H, d = Q.shape
+    return {"value": attn_flops(B, H, N, d) / (ms * 1e-3) / 1e12, "unit": "TFLOPS", "ms_per_step": ms,
+            "h2d_bytes_per_step": 3 * Q.numel() * Q.element_size(), "d2h_bytes_per_step": Q.numel() * Q.element_size(),
+            "steps": w_steps}
+
+
+def run_reference(args):
+    """The reference arm: the CPU oracle, as it stands, on a bounded sample per step.
+
+    Each step = oracle grouping (1 warm Lloyd iteration) + stable sort + quantizer
+    for head 0 of the Wan2.2-shaped workload, then oracle attention on R query
+    rows of that head against all N keys; the metric credits the attention
+    FLOPs of those rows (4 R N d) per step time.
+    """
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import numpy as np
+
+    import oracle
+    from bit_fp8_attention_means_gb300 import inputs
+    w = inputs.WORKLOADS["wan"]
+    N, d, k = w.N, w.d, w.k
+    Q, K, V = inputs.make_qkv(w, "cpu", H=1)
+    q, kk, v = (inputs.to_u16(t) for t in (Q, K, V))
+    cent, lab = oracle.kmeans(v, k, 1)                      # setup: a first (cold) clustering
+    rng = np.random.default_rng(0)
+    R = 64
+    rows = np.sort(rng.choice(N, R, replace=False)).astype(np.int32)
+
+    def step():
+        nonlocal cent
+        cent, lab = oracle.kmeans(v, k, 1, centroids=cent)
+        perm = oracle.argsort_labels(lab, k)
+        qz = oracle.quantize(q, kk, v, perm, 1)
+        oracle.attn(qz, N, rows=rows)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    val = 4.0 * R * N * d / dt / 1e12
+    sample = ("per step: oracle k-means (1 warm Lloyd iteration, k=%d) + argsort + quantizer on head 0 of the "
+              "Wan2.2-shaped workload (N=%d, d=%d), then oracle attention on %d query rows against all keys; "
+              "credited FLOPs = 4*R*N*d" % (k, N, d, R))
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOPS", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle; fp32 where codes are decided)",
+        "data": "synthetic: seeded Wan2.2-shaped head",
+        "config": {"workload": "wan2.2-shaped B=%d H=%d N=%d d=%d, k=%d" % (w.B, w.H, N, d, k),
+                   "step": "bounded CPU sample, see cpu_baseline.sample"},
+        "cpu_baseline": {"value": val, "unit": "TFLOPS", "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": val, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def run_schedule(args):
+    """Amortized denoising schedule: 50 steps, clustering only where the schedule says."""
+    import torch
+
+    from bit_fp8_attention_means_gb300 import inputs, schedule
+    dev = torch.device("cuda", 0)
+    w = inputs.WORKLOADS["wan"]
+    S = 50
+    Q, K, V = inputs.make_qkv(w, dev)
+    state = schedule.GroupingState()
+    times = schedule.StepTimes()
+    qz = O = None
+    for s in range(S):
+        if s > 0:
+            V = inputs.drift_v(V, s, w.seed)
+            Q, K, _ = inputs.make_qkv(w, dev, seed=w.seed + 100 + s, H=w.H)
+        qz, O = schedule.run_step(state, Q, K, V, s, S, w.k, w.iters, 1, qz=qz, O=O, times=times)
+        torch.cuda.synchronize()
+        schedule.collect(times)
+    tot = sum(times.cluster_ms) + sum(times.quantize_ms) + sum(times.attn_ms)
+    flops = attn_flops(w.B, w.H, w.N, w.d)
+    print(json.dumps({
+        "mode": "schedule", "metric": METRIC, "steps": S, "clusterings": state.clusterings,
+        "cluster_steps": [s for s in range(S) if schedule.clusters_at(s, S)],
+        "cluster_share_of_path": sum(times.cluster_ms) / tot,
+        "cluster_ms_per_grouping_step": sum(times.cluster_ms[1:]) / max(1, state.clusterings - 1),
+        "cold_cluster_ms": times.cluster_ms[0],
+        "quantize_ms_mean": statistics.mean(times.quantize_ms), "attn_ms_mean": statistics.mean(times.attn_ms),
+        "amortized_tflops": S * flops / (tot * 1e-3) / 1e12,
+        "config": {"workload": "wan2.2-shaped 50-step schedule, V drift N(0,0.05), Q/K redrawn"}}), flush=True)
+
+
+def run_sweep(args):
+    """Attention kernel alone, H=24, N in {4K..128K}, ExpCast x V-Smooth on/off."""
+    import torch
+
+    from bit_fp8_attention_means_gb300 import inputs, vc
+    dev = torch.device("cuda", 0)
+    rows = []
+    for N in (4096, 16384, 32768, 65536, 131072):
+        w = inputs.sweep_workload(N)
+        Q, K, V = inputs.make_qkv(w, dev)
+        perm = vc.vc_cluster(V, w.k, w.iters)[2]
+        s = vc.shape_of(Q)
+        O = torch.empty_like(Q)
+        flops = attn_flops(w.B, w.H, N, w.d)
+        for vs in (0, 1):
+            qz = vc.vc_quantize(Q, K, V, perm if vs else None, vs)
+            for ec in (0, 1):
+                for _ in range(2):
+                    vc.vc_attn_fwd(qz, s, expcast=ec, vsmooth=vs, O=O)
+                torch.cuda.synchronize()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                reps = max(2, int(2e14 // flops))
+                e0.record()
+                for _ in range(reps):
+                    vc.vc_attn_fwd(qz, s, expcast=ec, vsmooth=vs, O=O)
+                e1.record()
+                torch.cuda.synchronize()
+                ms = e0.elapsed_time(e1) / reps
+                rows.append({"N": N, "expcast": ec, "vsmooth": vs, "ms": ms, "tflops": flops / ms / 1e9})
+        del Q, K, V, qz, O
+        torch.cuda.empty_cache()
+    print(json.dumps({"mode": "sweep", "metric": "attention kernel TFLOPS, H=24 d=128", "rows": rows}), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    if args.mode == "step":
+        run_ours(args)
+    elif args.mode == "schedule":
+        run_schedule(args)
+    else:
+        run_sweep(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,128 @@
+// vc_api.cu -- the extern "C" entry points declared in include/vc.h.
+// Argument checks happen here, on the host, before anything is enqueued.
+#include <cstdint>
+
+#include "vc.h"
+#include "vc_internal.h"
+
+namespace vc {
+
+vc_status cuda_status(cudaError_t e) { return e == cudaSuccess ? VC_OK : VC_ERR_CUDA; }
+
+vc_status check_shape(const vc_shape& s) {
+    if (s.B < 1 || s.H < 1 || s.N < 1 || s.d < 1) return VC_ERR_INVALID_ARG;
+    if (s.d != 64 && s.d != 128) return VC_ERR_UNSUPPORTED;
+    if (s.N > (1 << 24)) return VC_ERR_UNSUPPORTED;
+    if (s.s_b <= 0 || s.s_n <= 0 || s.s_h <= 0) return VC_ERR_INVALID_ARG;
+    if ((s.s_b % 8) || (s.s_n % 8) || (s.s_h % 8)) return VC_ERR_INVALID_ARG;
+    // TMA row coordinates are 32-bit
+    if ((int64_t)s.B * s.H * npad_of(s.N) >= (int64_t(1) << 31)) return VC_ERR_UNSUPPORTED;
+    return VC_OK;
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace vc
+
+using namespace vc;
+
+extern "C" {
+
+const char* vc_status_string(vc_status s) {
+    switch (s) {
+        case VC_OK: return "VC_OK";
+        case VC_ERR_INVALID_ARG: return "VC_ERR_INVALID_ARG";
+        case VC_ERR_UNSUPPORTED: return "VC_ERR_UNSUPPORTED";
+        case VC_ERR_WORKSPACE: return "VC_ERR_WORKSPACE";
+        case VC_ERR_CUDA: return "VC_ERR_CUDA";
+        case VC_ERR_TIMEOUT: return "VC_ERR_TIMEOUT";
+    }
+    return "VC_ERR_UNKNOWN";
+}
+
+int vc_version(void) { return 100; }
+
+size_t vc_cluster_workspace(vc_shape shape, int k) {
+    if (check_shape(shape) != VC_OK || k < 1) return 0;
+    return cluster_workspace(shape, k);
+}
+
+vc_status vc_cluster(const void* V, vc_shape shape, int k, int iters, int warm_start, float* centroids,
+                     int32_t* labels, int32_t* perm, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                     vc_stream_t stream) {
+    vc_status st = check_shape(shape);
+    if (st != VC_OK) return st;
+    if (!V || !centroids || !labels || !perm) return VC_ERR_INVALID_ARG;
+    if (!aligned16(V)) return VC_ERR_INVALID_ARG;
+    if (iters < 1 || (warm_start != 0 && warm_start != 1)) return VC_ERR_INVALID_ARG;
+    if (k < 1 || k > 1024) return VC_ERR_UNSUPPORTED;
+    if (k > shape.N) return VC_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < cluster_workspace(shape, k) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return VC_ERR_WORKSPACE;
+    return launch_cluster(static_cast<const uint16_t*>(V), shape, k, iters, warm_start, centroids, labels, perm,
+                          workspace, dev_status, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t vc_quantize_workspace(vc_shape shape) {
+    if (check_shape(shape) != VC_OK) return 0;
+    return quantize_workspace(shape);
+}
+
+vc_status vc_quantize(const void* Q, const void* K, const void* V, vc_shape shape, const int32_t* perm, int vsmooth,
+                      uint8_t* Q8, float* sq, uint8_t* K8, float* sk, uint8_t* V8T, float* sv, void* mu,
+                      void* workspace, size_t workspace_bytes, vc_stream_t stream) {
+    vc_status st = check_shape(shape);
+    if (st != VC_OK) return st;
+    if (vsmooth != 0 && vsmooth != 1) return VC_ERR_INVALID_ARG;
+    if (!Q || !K || !V || !Q8 || !sq || !K8 || !sk || !V8T || !sv || (vsmooth && !mu)) return VC_ERR_INVALID_ARG;
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(Q8) || !aligned16(K8) || !aligned16(V8T))
+        return VC_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < quantize_workspace(shape) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return VC_ERR_WORKSPACE;
+    return launch_quantize(static_cast<const uint16_t*>(Q), static_cast<const uint16_t*>(K),
+                           static_cast<const uint16_t*>(V), shape, perm, vsmooth, Q8, sq, K8, sk, V8T, sv,
+                           static_cast<uint16_t*>(mu), workspace, reinterpret_cast<cudaStream_t>(stream));
+}
+
+static vc_status attn_common(const uint8_t* Q8, const float* sq, const uint8_t* K8, const float* sk,
+                             const uint8_t* V8T, const float* sv, const void* mu, const vc_shape& shape,
+                             int expcast, int vsmooth, void* O) {
+    vc_status st = check_shape(shape);
+    if (st != VC_OK) return st;
+    if ((expcast != 0 && expcast != 1) || (vsmooth != 0 && vsmooth != 1)) return VC_ERR_INVALID_ARG;
+    if (!Q8 || !sq || !K8 || !sk || !V8T || !sv || !O || (vsmooth && !mu)) return VC_ERR_INVALID_ARG;
+    if (!aligned16(Q8) || !aligned16(K8) || !aligned16(V8T) || !aligned16(O)) return VC_ERR_INVALID_ARG;
+    return VC_OK;
+}
+
+vc_status vc_attn_fwd(const uint8_t* Q8, const float* sq, const uint8_t* K8, const float* sk, const uint8_t* V8T,
+                      const float* sv, const void* mu, vc_shape shape, float softmax_scale, int expcast, int vsmooth,
+                      void* O, int32_t* dev_status, vc_stream_t stream) {
+    vc_status st = attn_common(Q8, sq, K8, sk, V8T, sv, mu, shape, expcast, vsmooth, O);
+    if (st != VC_OK) return st;
+    return launch_attn(Q8, sq, K8, sk, V8T, sv, static_cast<const uint16_t*>(mu), shape, softmax_scale, expcast,
+                       vsmooth, static_cast<uint16_t*>(O), dev_status, reinterpret_cast<cudaStream_t>(stream),
+                       nullptr);
+}
+
+vc_status vc_attn_fwd_debug(const uint8_t* Q8, const float* sq, const uint8_t* K8, const float* sk,
+                            const uint8_t* V8T, const float* sv, const void* mu, vc_shape shape, float softmax_scale,
+                            int expcast, int vsmooth, void* O, int32_t* dev_status, vc_stream_t stream, int dbg_bh,
+                            int dbg_qtile, float* S_dump, uint8_t* P_dump) {
+    vc_status st = attn_common(Q8, sq, K8, sk, V8T, sv, mu, shape, expcast, vsmooth, O);
+    if (st != VC_OK) return st;
+    if (!S_dump || !P_dump || dbg_bh < 0 || dbg_bh >= shape.B * shape.H || dbg_qtile < 0 ||
+        dbg_qtile >= nblk_of(shape.N))
+        return VC_ERR_INVALID_ARG;
+    AttnDebug dbg;
+    dbg.bh = dbg_bh;
+    dbg.qtile = dbg_qtile;
+    dbg.S = S_dump;
+    dbg.P = P_dump;
+    return launch_attn(Q8, sq, K8, sk, V8T, sv, static_cast<const uint16_t*>(mu), shape, softmax_scale, expcast,
+                       vsmooth, static_cast<uint16_t*>(O), dev_status, reinterpret_cast<cudaStream_t>(stream), &dbg);
+}
+
+}  // extern "C"

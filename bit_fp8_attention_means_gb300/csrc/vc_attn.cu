@@ -1,0 +1,602 @@
+// vc_attn.cu -- FP8 attention forward with ExpCast-FP8 and the V-Smooth mean
+// restore, on tcgen05 tensor cores (sm_103a).
+//
+// What it computes: paper summary (paper.rainbus.top), 前置知识 "在线 softmax"
+// (running max m_i, normaliser l_i, numerator A_i, rescale alpha_i) and
+// 方法步骤详情 steps 3-4 (A_i <- alpha_i A_i + P_q,ij R_q,j + r_ij mu_j^T with
+// r_ij the row sum of the quantized probabilities; ExpCast byte
+// c = clip(Round(8(u+8)+56+beta), 0, 120)); dimensionstp.github.io 2-3 / 2-4.
+//
+// One CTA = 128 query rows of one (b, h); 10 warps:
+//   warps 0-7  softmax: two warpgroups; thread (wg, row) owns query row `row`
+//              and key columns [64 wg, 64 wg + 64) of each 128-key tile, and
+//              output channels [wg d/2, (wg+1) d/2).  The two halves of a row
+//              exchange their partial maxima through shared memory.
+//   warp 8     producer: TMA loads of Q (once), K and V^T tiles (ring of NS
+//              stages), and the block means mu_j converted to fp32.
+//   warp 9     MMA issuer (one thread) and TMEM owner.
+// Tensor memory (512 columns):
+//   S0, S1 [0,256)     fp32 scores of tiles j (double-buffered), QK^T.
+//   P      inside S    the probability bytes of tile j overwrite the first 16
+//                      columns of each half of the score buffer they came from.
+//   O      [256,256+d) fp32 residual accumulator A_res (units of codes).
+//   R      16 columns  r_ij = P_j * 1 from a small MMA against a ones operand.
+// Per key tile j the MMA thread issues QK(j+1) before PV(j), so the tensor
+// core computes the next scores while the softmax warps turn tile j into bytes.
+//
+// The mean term is kept in registers: M <- alpha (M + r_{j-1} mu_{j-1}), applied
+// lazily one tile late, when r_{j-1} has come back from the row-sum MMA; O in
+// TMEM is rescaled only when some row of the warp raised its maximum.  Final
+// output O = (s_v (.) A_res + M) / l.
+//
+// ExpCast inner loop, per score: ts = sat(acc * sigma/16 + C/128) (one FFMA
+// with saturation = clip to [0, 128] of t/128, exact because /128 and /16 are
+// powers of two), then b = ts*128 + 1.5*2^23 (packed FFMA2) whose low byte is
+// rint(t), then byte packing with PRMT.  The upper clip at 120 is implied
+// while |m'| < 2^19 (t <= 119.65 + 2^-1); rows beyond take a path with an
+// explicit min.
+#include <cstdio>
+
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+
+#include "vc_device.cuh"
+#include "vc_internal.h"
+
+namespace vc {
+namespace {
+
+constexpr int kThreads = 320;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23: adding it rounds to an integer in the low mantissa bits
+
+template <int D>
+struct Cfg {
+    static constexpr int NS = (D == 128) ? 4 : 6;
+    static constexpr int QB = 128 * D;
+    static constexpr int KB = 128 * D;
+    static constexpr int VB = D * 128;
+    static constexpr uint32_t QK_SWZ = (D == 128) ? kSwizzle128B : kSwizzle64B;
+    static constexpr uint32_t QK_SBO = 8 * D;  // bytes per group of 8 rows
+    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_K = OFF_Q + QB;
+    static constexpr int OFF_V = OFF_K + NS * KB;
+    static constexpr int OFF_ONES = OFF_V + NS * VB;
+    static constexpr int OFF_MU = OFF_ONES + 2048;
+    static constexpr int OFF_XCH = OFF_MU + NS * D * 4;
+    static constexpr int OFF_BAR = OFF_XCH + 2 * 2 * 128 * 4;
+    static constexpr int NBAR = 32;
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+    static constexpr int USED = OFF_MISC + 64;
+    // at least 116 KB so that exactly one CTA (and one 512-column TMEM owner) sits on an SM
+    static constexpr int SMEM = ((USED > 118784) ? USED : 118784) + 1024;
+    // barrier indices
+    static constexpr int B_Q = 0;
+    static constexpr int B_KVF = 1;
+    static constexpr int B_KVE = B_KVF + NS;
+    static constexpr int B_MUE = B_KVE + NS;
+    static constexpr int B_SF = B_MUE + NS;
+    static constexpr int B_PF = B_SF + 2;
+    static constexpr int B_OD = B_PF + 2;
+    static constexpr int B_XCH = B_OD + 1;
+    static constexpr int B_TD = B_XCH + 2;
+    static constexpr int NBAR_USED = B_TD + 1;
+    static_assert(NBAR_USED <= NBAR, "barrier area");
+    // TMEM columns
+    static constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O = 256, COL_R = 256 + D;
+    static_assert(COL_R + 16 <= kTmemCols, "tmem budget");
+};
+
+struct AttnParams {
+    const float* sq;
+    const float* sk;
+    const float* sv;
+    const uint16_t* mu;
+    uint16_t* O;
+    int64_t o_sb, o_sn, o_sh;
+    int H, N, nblk;
+    int64_t Npad;
+    float kscale;
+    int32_t* dev_status;
+    uint64_t timeout_ns;
+    int dbg_bh, dbg_qtile;
+    float* S_dump;
+    uint8_t* P_dump;
+};
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Bounded wait that ignores the abort flag: used at teardown to let this
+// CTA's own copies and MMAs in flight finish before their memory is released.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t timeout_ns) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer_ns() - t0 > timeout_ns) return;
+    }
+}
+
+template <int D, bool EXPCAST, bool VSMOOTH, bool DBG>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
+    using C = Cfg<D>;
+    constexpr int NS = C::NS;
+    constexpr int HD = D / 2;  // output channels per softmax thread
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    auto bar = [&](int i) -> uint32_t { return sbase + C::OFF_BAR + 8u * (uint32_t)i; };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 16);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int qtile = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int bh = b * p.H + h;
+    const int J = p.nblk;
+    const uint64_t tmo = p.timeout_ns;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(C::B_Q), 1);
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(bar(C::B_KVF + s), 1);
+            mbar_init(bar(C::B_KVE + s), 1);
+            mbar_init(bar(C::B_MUE + s), 8);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(C::B_SF + i), 1);
+            mbar_init(bar(C::B_PF + i), 8);
+            mbar_init(bar(C::B_XCH + i), 256);
+        }
+        mbar_init(bar(C::B_OD), 1);
+        mbar_init(bar(C::B_TD), 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    if (threadIdx.x < 256) {
+        // ones operand for the row-sum MMA: row 0 = E4M3 1.0 (0x38), rows 1..15 = 0
+        const uint64_t v = (threadIdx.x < 16) ? 0x3838383838383838ull : 0ull;
+        *reinterpret_cast<uint64_t*>(smem + C::OFF_ONES + threadIdx.x * 8) = v;
+        fence_proxy_async_smem();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == kProducerWarp) {
+        // ------------------------------------------------------------ producer
+        const int32_t row0 = (int32_t)((int64_t)bh * p.Npad);
+        if (lane == 0) {
+            prefetch_tensormap(&tmQ);
+            prefetch_tensormap(&tmK);
+            prefetch_tensormap(&tmV);
+            mbar_expect_tx(bar(C::B_Q), C::QB);
+            tma_load_2d(sbase + C::OFF_Q, &tmQ, 0, row0 + qtile * 128, bar(C::B_Q));
+            mbar_arrive(bar(C::B_Q));
+        }
+        int issued = 0;
+        for (int j = 0; j < J; ++j) {
+            const int s = j % NS, n = j / NS;
+            if (j >= NS) {
+                if (!mbar_wait(bar(C::B_KVE + s), (n - 1) & 1, abort_flag, p.dev_status, tmo)) break;
+                if (VSMOOTH && !mbar_wait(bar(C::B_MUE + s), (n - 1) & 1, abort_flag, p.dev_status, tmo)) break;
+            }
+            if (lane == 0) {
+                mbar_expect_tx(bar(C::B_KVF + s), C::KB + C::VB);
+                tma_load_2d(sbase + C::OFF_K + s * C::KB, &tmK, 0, row0 + j * 128, bar(C::B_KVF + s));
+                tma_load_2d(sbase + C::OFF_V + s * C::VB, &tmV, j * 128, bh * D, bar(C::B_KVF + s));
+            }
+            if (VSMOOTH) {
+                constexpr int PER = D / 32;
+                const uint16_t* src = p.mu + ((int64_t)bh * p.nblk + j) * D + lane * PER;
+                float* dst = reinterpret_cast<float*>(smem + C::OFF_MU + s * D * 4) + lane * PER;
+                if (PER == 4) {
+                    const uint2 w = __ldg(reinterpret_cast<const uint2*>(src));
+                    *reinterpret_cast<float4*>(dst) =
+                        make_float4(bf16_bits_to_f32(w.x & 0xFFFFu), bf16_bits_to_f32(w.x >> 16),
+                                    bf16_bits_to_f32(w.y & 0xFFFFu), bf16_bits_to_f32(w.y >> 16));
+                } else {
+                    const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(src));
+                    *reinterpret_cast<float2*>(dst) =
+                        make_float2(bf16_bits_to_f32(w & 0xFFFFu), bf16_bits_to_f32(w >> 16));
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::B_KVF + s));
+            issued = j + 1;
+        }
+        // let this CTA's own copies in flight land before the CTA can exit
+        for (int j = (issued > NS ? issued - NS : 0); j < issued; ++j)
+            drain_wait(bar(C::B_KVF + j % NS), (j / NS) & 1, tmo);
+        drain_wait(bar(C::B_Q), 0, tmo);
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t IDESC_QK = idesc_f8_e4m3(128, 128);
+            constexpr uint32_t IDESC_PV = idesc_f8_e4m3(128, D);
+            constexpr uint32_t IDESC_RS = idesc_f8_e4m3(128, 16);
+            auto issue_qk = [&](int j) {
+                const int s = j % NS;
+                const uint32_t d = tmem + ((j & 1) ? C::COL_S1 : C::COL_S0);
+#pragma unroll
+                for (int kk = 0; kk < D / 32; ++kk) {
+                    const uint64_t ad = smem_desc(sbase + C::OFF_Q + kk * 32, C::QK_SBO, C::QK_SWZ);
+                    const uint64_t bd = smem_desc(sbase + C::OFF_K + s * C::KB + kk * 32, C::QK_SBO, C::QK_SWZ);
+                    mma_f8_ss(d, ad, bd, IDESC_QK, kk > 0 ? 1u : 0u);
+                }
+            };
+            auto issue_pv_rs = [&](int j) {
+                const int s = j % NS;
+                const uint32_t pbase = tmem + ((j & 1) ? C::COL_S1 : C::COL_S0);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint32_t a = pbase + (kk < 2 ? kk * 8 : 64 + (kk - 2) * 8);
+                    const uint64_t bd = smem_desc(sbase + C::OFF_V + s * C::VB + kk * 32, 1024, kSwizzle128B);
+                    mma_f8_ts(tmem + C::COL_O, a, bd, IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+                }
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint32_t a = pbase + (kk < 2 ? kk * 8 : 64 + (kk - 2) * 8);
+                    const uint64_t bd = smem_desc(sbase + C::OFF_ONES + kk * 32, 1024, kSwizzle128B);
+                    mma_f8_ts(tmem + C::COL_R, a, bd, IDESC_RS, kk > 0 ? 1u : 0u);
+                }
+            };
+            bool ok = mbar_wait(bar(C::B_Q), 0, abort_flag, p.dev_status, tmo) &&
+                      mbar_wait(bar(C::B_KVF), 0, abort_flag, p.dev_status, tmo);
+            if (ok) {
+                tc_fence_after();
+                issue_qk(0);
+                mma_commit(bar(C::B_SF + 0));
+            }
+            for (int j = 0; ok && j < J; ++j) {
+                if (j + 1 < J) {
+                    const int s1 = (j + 1) % NS;
+                    if (!mbar_wait(bar(C::B_KVF + s1), ((j + 1) / NS) & 1, abort_flag, p.dev_status, tmo)) break;
+                    tc_fence_after();
+                    issue_qk(j + 1);
+                    mma_commit(bar(C::B_SF + ((j + 1) & 1)));
+                }
+                if (!mbar_wait(bar(C::B_PF + (j & 1)), (j >> 1) & 1, abort_flag, p.dev_status, tmo)) break;
+                tc_fence_after();
+                issue_pv_rs(j);
+                mma_commit(bar(C::B_OD));
+                mma_commit(bar(C::B_KVE + j % NS));
+            }
+            // every MMA this thread issued has completed once this phase flips
+            mma_commit(bar(C::B_TD));
+            drain_wait(bar(C::B_TD), 0, tmo);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ softmax / correction / epilogue
+        const int wg = warp >> 2, q = warp & 3;
+        const int row = q * 32 + lane;
+        const uint32_t lane_addr = tmem + ((uint32_t)(q * 32) << 16);
+        const int qrow = qtile * 128 + row;
+        const float sq_i = __ldg(p.sq + (int64_t)bh * p.nblk + qtile);
+        const int tail = p.N - (J - 1) * 128;  // valid keys of the last tile, 1..128
+        const bool dbg_cta = DBG && bh == p.dbg_bh && qtile == p.dbg_qtile;
+        float* xch = reinterpret_cast<float*>(smem + C::OFF_XCH);
+        float m = -INFINITY, l = 0.f;
+        float macc[HD];
+#pragma unroll
+        for (int c = 0; c < HD; ++c) macc[c] = 0.f;
+        float sk_next = __ldg(p.sk + (int64_t)bh * p.nblk);
+        bool ok = true;
+        for (int j = 0; j < J; ++j) {
+            const int sb = j & 1;
+            const uint32_t colS = sb ? C::COL_S1 : C::COL_S0;
+            const float sk_j = sk_next;
+            if (j + 1 < J) sk_next = __ldg(p.sk + (int64_t)bh * p.nblk + j + 1);
+            if (!mbar_wait(bar(C::B_SF + sb), (j >> 1) & 1, abort_flag, p.dev_status, tmo)) { ok = false; break; }
+            if (VSMOOTH && !mbar_wait(bar(C::B_KVF + j % NS), (j / NS) & 1, abort_flag, p.dev_status, tmo)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            float a[64];
+            {
+                uint32_t r0[32], r1[32];
+                tmem_ld32(lane_addr + colS + wg * 64, r0);
+                tmem_ld32(lane_addr + colS + wg * 64 + 32, r1);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    a[i] = __uint_as_float(r0[i]);
+                    a[32 + i] = __uint_as_float(r1[i]);
+                }
+            }
+            if (dbg_cta) {
+                float* dst = p.S_dump + (int64_t)row * p.Npad + j * 128 + wg * 64;
+#pragma unroll
+                for (int i = 0; i < 64; ++i) dst[i] = a[i];
+            }
+            const bool masked = (j == J - 1) && (tail < 128);
+            if (masked) {
+#pragma unroll
+                for (int i = 0; i < 64; ++i)
+                    if (wg * 64 + i >= tail) a[i] = -INFINITY;
+            }
+            // partial row max over this thread's 64 keys
+            float mx;
+            {
+                float t[22];
+#pragma unroll
+                for (int i = 0; i < 21; ++i) t[i] = max3(a[3 * i], a[3 * i + 1], a[3 * i + 2]);
+                t[21] = a[63];
+                float u[8];
+#pragma unroll
+                for (int i = 0; i < 7; ++i) u[i] = max3(t[3 * i], t[3 * i + 1], t[3 * i + 2]);
+                u[7] = t[21];
+                mx = max3(max3(u[0], u[1], u[2]), max3(u[3], u[4], u[5]), fmaxf(u[6], u[7]));
+            }
+            xch[sb * 256 + wg * 128 + row] = mx;
+            mbar_arrive(bar(C::B_XCH + sb));
+            if (!mbar_wait(bar(C::B_XCH + sb), (j >> 1) & 1, abort_flag, p.dev_status, tmo)) { ok = false; break; }
+            const float mx_all = fmaxf(mx, xch[sb * 256 + (1 - wg) * 128 + row]);
+            const float sigma = __fmul_rn(__fmul_rn(sq_i, sk_j), p.kscale);
+            const float m_new = fmaxf(m, __fmul_rn(sigma, mx_all));
+            const float alpha = ex2_approx(m - m_new);
+            uint32_t pw[16];
+            if (EXPCAST) {
+                const float Cc = __fmaf_rn(-8.f, m_new, 119.65f);
+                const float k1 = sigma * 0.0625f;
+                const float k2 = Cc * 0.0078125f;
+                const bool fast = fabsf(m_new) < 524288.f;
+#pragma unroll
+                for (int w = 0; w < 16; ++w) {
+                    const float t0 = fma_sat(a[4 * w + 0], k1, k2);
+                    const float t1 = fma_sat(a[4 * w + 1], k1, k2);
+                    const float t2 = fma_sat(a[4 * w + 2], k1, k2);
+                    const float t3 = fma_sat(a[4 * w + 3], k1, k2);
+                    const float2 b01 = __ffma2_rn(make_float2(t0, t1), make_float2(128.f, 128.f),
+                                                  make_float2(kMagic, kMagic));
+                    const float2 b23 = __ffma2_rn(make_float2(t2, t3), make_float2(128.f, 128.f),
+                                                  make_float2(kMagic, kMagic));
+                    uint32_t u0 = __float_as_uint(b01.x), u1 = __float_as_uint(b01.y);
+                    uint32_t u2 = __float_as_uint(b23.x), u3 = __float_as_uint(b23.y);
+                    if (!fast) {
+                        u0 = min(u0 & 0xFFu, 120u);
+                        u1 = min(u1 & 0xFFu, 120u);
+                        u2 = min(u2 & 0xFFu, 120u);
+                        u3 = min(u3 & 0xFFu, 120u);
+                    }
+                    pw[w] = prmt(prmt(u0, u1, 0x0040u), prmt(u2, u3, 0x0040u), 0x5410u);
+                }
+            } else {
+                const float off = __fsub_rn(8.f, m_new);
+#pragma unroll
+                for (int w = 0; w < 16; ++w) {
+                    const float e0 = ex2_approx(__fmaf_rn(a[4 * w + 0], sigma, off));
+                    const float e1 = ex2_approx(__fmaf_rn(a[4 * w + 1], sigma, off));
+                    const float e2 = ex2_approx(__fmaf_rn(a[4 * w + 2], sigma, off));
+                    const float e3 = ex2_approx(__fmaf_rn(a[4 * w + 3], sigma, off));
+                    pw[w] = cvt_e4m3x2(e0, e1) | (cvt_e4m3x2(e2, e3) << 16);
+                }
+            }
+            if (masked) {
+#pragma unroll
+                for (int w = 0; w < 16; ++w) {
+                    uint32_t keep = 0;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        if (wg * 64 + 4 * w + e < tail) keep |= 0xFFu << (8 * e);
+                    pw[w] &= keep;
+                }
+            }
+            if (dbg_cta) {
+                uint32_t* dst = reinterpret_cast<uint32_t*>(p.P_dump + (int64_t)row * p.Npad + j * 128 + wg * 64);
+#pragma unroll
+                for (int w = 0; w < 16; ++w) dst[w] = pw[w];
+            }
+            tmem_st16(lane_addr + colS + wg * 64, pw);
+            tmem_wait_st();
+            if (j > 0) {
+                if (!mbar_wait(bar(C::B_OD), (j - 1) & 1, abort_flag, p.dev_status, tmo)) { ok = false; break; }
+                tc_fence_after();
+                uint32_t rbits;
+                tmem_ld1(lane_addr + C::COL_R, rbits);
+                tmem_wait_ld();
+                const float r_prev = __uint_as_float(rbits);
+                const bool rescale = __any_sync(0xffffffffu, alpha != 1.f);
+                if (VSMOOTH) {
+                    const float* mu_prev =
+                        reinterpret_cast<const float*>(smem + C::OFF_MU + ((j - 1) % NS) * D * 4) + wg * HD;
+#pragma unroll
+                    for (int c = 0; c < HD; c += 4) {
+                        const float4 mv = *reinterpret_cast<const float4*>(mu_prev + c);
+                        macc[c + 0] = __fmaf_rn(r_prev, mv.x, macc[c + 0]);
+                        macc[c + 1] = __fmaf_rn(r_prev, mv.y, macc[c + 1]);
+                        macc[c + 2] = __fmaf_rn(r_prev, mv.z, macc[c + 2]);
+                        macc[c + 3] = __fmaf_rn(r_prev, mv.w, macc[c + 3]);
+                    }
+                    if (rescale) {
+#pragma unroll
+                        for (int c = 0; c < HD; ++c) macc[c] *= alpha;
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(C::B_MUE + (j - 1) % NS));
+                }
+                l = alpha * (l + r_prev);
+                if (rescale) {
+#pragma unroll
+                    for (int c0 = 0; c0 < HD; c0 += 32) {
+                        uint32_t o[32];
+                        tmem_ld32(lane_addr + C::COL_O + wg * HD + c0, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                        tmem_st32(lane_addr + C::COL_O + wg * HD + c0, o);
+                    }
+                    tmem_wait_st();
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::B_PF + sb));
+            m = m_new;
+        }
+        if (ok && mbar_wait(bar(C::B_OD), (J - 1) & 1, abort_flag, p.dev_status, tmo)) {
+            tc_fence_after();
+            uint32_t rbits;
+            tmem_ld1(lane_addr + C::COL_R, rbits);
+            tmem_wait_ld();
+            const float r_last = __uint_as_float(rbits);
+            l += r_last;
+            if (VSMOOTH) {
+                const float* mu_last =
+                    reinterpret_cast<const float*>(smem + C::OFF_MU + ((J - 1) % NS) * D * 4) + wg * HD;
+#pragma unroll
+                for (int c = 0; c < HD; ++c) macc[c] = __fmaf_rn(r_last, mu_last[c], macc[c]);
+            }
+            const float inv_l = __frcp_rn(l);
+            const float* svp = p.sv + (int64_t)bh * D + wg * HD;
+            uint16_t* dst = p.O + (int64_t)b * p.o_sb + (int64_t)qrow * p.o_sn + (int64_t)h * p.o_sh + wg * HD;
+#pragma unroll
+            for (int c0 = 0; c0 < HD; c0 += 32) {
+                uint32_t o[32];
+                tmem_ld32(lane_addr + C::COL_O + wg * HD + c0, o);
+                tmem_wait_ld();
+                uint32_t packed[16];
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) {
+                    const float v0 = __fmaf_rn(__ldg(svp + c0 + i), __uint_as_float(o[i]), macc[c0 + i]) * inv_l;
+                    const float v1 =
+                        __fmaf_rn(__ldg(svp + c0 + i + 1), __uint_as_float(o[i + 1]), macc[c0 + i + 1]) * inv_l;
+                    const __nv_bfloat162 pr = __floats2bfloat162_rn(v0, v1);
+                    packed[i / 2] = *reinterpret_cast<const uint32_t*>(&pr);
+                }
+                if (qrow < p.N) {
+                    uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v)
+                        d4[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+
+// cuTensorMapEncodeTiled is a driver API; it is looked up through the runtime
+// so that the library does not link against libcuda directly.
+PFN_cuTensorMapEncodeTiled_v12000 encode_tiled_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+bool make_map_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t row_bytes,
+                 uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swz) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_tiled_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {inner, rows};
+    const cuuint64_t strides[1] = {row_bytes};
+    const cuuint32_t box[2] = {box_inner, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int D, bool E, bool S, bool G>
+vc_status launch_one(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const AttnParams& p,
+                     dim3 grid, cudaStream_t st) {
+    auto kern = attn_fwd_kernel<D, E, S, G>;
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::SMEM);
+        if (e != cudaSuccess) return cuda_status(e);
+        attr = true;
+    }
+    kern<<<grid, kThreads, Cfg<D>::SMEM, st>>>(mq, mk, mv, p);
+    return cuda_status(cudaGetLastError());
+}
+
+template <int D>
+vc_status launch_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const AttnParams& p,
+                   dim3 grid, cudaStream_t st, int expcast, int vsmooth, bool dbg) {
+    if (dbg) {
+        if (expcast)
+            return vsmooth ? launch_one<D, true, true, true>(mq, mk, mv, p, grid, st)
+                           : launch_one<D, true, false, true>(mq, mk, mv, p, grid, st);
+        return vsmooth ? launch_one<D, false, true, true>(mq, mk, mv, p, grid, st)
+                       : launch_one<D, false, false, true>(mq, mk, mv, p, grid, st);
+    }
+    if (expcast)
+        return vsmooth ? launch_one<D, true, true, false>(mq, mk, mv, p, grid, st)
+                       : launch_one<D, true, false, false>(mq, mk, mv, p, grid, st);
+    return vsmooth ? launch_one<D, false, true, false>(mq, mk, mv, p, grid, st)
+                   : launch_one<D, false, false, false>(mq, mk, mv, p, grid, st);
+}
+
+}  // namespace
+
+vc_status launch_attn(const uint8_t* Q8, const float* sq, const uint8_t* K8, const float* sk, const uint8_t* V8T,
+                      const float* sv, const uint16_t* mu, const vc_shape& s, float softmax_scale, int expcast,
+                      int vsmooth, uint16_t* O, int32_t* dev_status, cudaStream_t st, const AttnDebug* dbg) {
+    const int nblk = nblk_of(s.N);
+    const int64_t Npad = npad_of(s.N);
+    const uint64_t rows_qk = (uint64_t)s.B * s.H * Npad;
+    const uint64_t rows_v = (uint64_t)s.B * s.H * s.d;
+    CUtensorMap mq, mk, mv;
+    const CUtensorMapSwizzle qk_swz = (s.d == 128) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    if (!make_map_2d(&mq, Q8, s.d, rows_qk, s.d, s.d, 128, qk_swz) ||
+        !make_map_2d(&mk, K8, s.d, rows_qk, s.d, s.d, 128, qk_swz) ||
+        !make_map_2d(&mv, V8T, Npad, rows_v, Npad, 128, s.d, CU_TENSOR_MAP_SWIZZLE_128B))
+        return VC_ERR_CUDA;
+    AttnParams p{};
+    p.sq = sq;
+    p.sk = sk;
+    p.sv = sv;
+    p.mu = mu;
+    p.O = O;
+    p.o_sb = s.s_b;
+    p.o_sn = s.s_n;
+    p.o_sh = s.s_h;
+    p.H = s.H;
+    p.N = s.N;
+    p.nblk = nblk;
+    p.Npad = Npad;
+    const double sc = softmax_scale > 0.f ? (double)softmax_scale : (double)(float)(1.0 / __builtin_sqrt((double)s.d));
+    p.kscale = (float)(sc * 1.4426950408889634);
+    p.dev_status = dev_status;
+    p.timeout_ns = 4000000000ull;
+    p.dbg_bh = dbg ? dbg->bh : -1;
+    p.dbg_qtile = dbg ? dbg->qtile : -1;
+    p.S_dump = dbg ? dbg->S : nullptr;
+    p.P_dump = dbg ? dbg->P : nullptr;
+    const dim3 grid(nblk, s.H, s.B);
+    if (s.d == 128) return launch_d<128>(mq, mk, mv, p, grid, st, expcast, vsmooth, dbg != nullptr);
+    return launch_d<64>(mq, mk, mv, p, grid, st, expcast, vsmooth, dbg != nullptr);
+}
+
+}  // namespace vc

@@ -1,0 +1,39 @@
+// vc_internal.h -- host-side declarations shared by the library's translation units.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "vc.h"
+
+namespace vc {
+
+constexpr int kBlock = 128;  // tokens per block (B_v) and per attention tile
+
+inline int nblk_of(int N) { return (N + kBlock - 1) / kBlock; }
+inline int64_t npad_of(int N) { return (int64_t)nblk_of(N) * kBlock; }
+
+vc_status check_shape(const vc_shape& s);
+vc_status cuda_status(cudaError_t e);
+
+// quantizer (vc_quantize.cu)
+size_t quantize_workspace(const vc_shape& s);
+vc_status launch_quantize(const uint16_t* Q, const uint16_t* K, const uint16_t* V, const vc_shape& s,
+                          const int32_t* perm, int vsmooth, uint8_t* Q8, float* sq, uint8_t* K8, float* sk,
+                          uint8_t* V8T, float* sv, uint16_t* mu, void* ws, cudaStream_t st);
+
+// grouping (vc_cluster.cu)
+size_t cluster_workspace(const vc_shape& s, int k);
+vc_status launch_cluster(const uint16_t* V, const vc_shape& s, int k, int iters, int warm, float* cent,
+                         int32_t* labels, int32_t* perm, void* ws, int32_t* dev_status, cudaStream_t st);
+
+// attention (vc_attn.cu)
+struct AttnDebug {
+    int bh = -1, qtile = -1;
+    float* S = nullptr;
+    uint8_t* P = nullptr;
+};
+vc_status launch_attn(const uint8_t* Q8, const float* sq, const uint8_t* K8, const float* sk, const uint8_t* V8T,
+                      const float* sv, const uint16_t* mu, const vc_shape& s, float softmax_scale, int expcast,
+                      int vsmooth, uint16_t* O, int32_t* dev_status, cudaStream_t st, const AttnDebug* dbg);
+
+}  // namespace vc

@@ -1,0 +1,217 @@
+// vc_quantize.cu -- the fused quantizer of the V-Smooth path.
+//
+// Paper summary (paper.rainbus.top), 方法步骤详情 step 2 and 前置知识 "低比特
+// 量化与离群值"; dimensionstp.github.io section 2-2:
+//   Q, K' = K[pi]: one fp32 scale per 128-token block, codes = E4M3(x * 448/amax).
+//   V' = V[pi]:   mu_j = bf16(block mean), R = V' - mu_j, residual codes with
+//                 one scale per channel over the whole head.
+// Three memory-bound kernels per call:
+//   quant_qk_kernel      Q and K' blocks (gathered rows for K'), one CTA per block.
+//   quant_v_stats_kernel block means of V' and the per-channel residual amax
+//                        (atomicMax on the fp32 bit pattern, values are >= 0).
+//   quant_v_codes_kernel residual codes, written token-contiguous per channel
+//                        (V8T [B,H,d,Npad]) so that the attention kernel can
+//                        read V as a K-major MMA operand.
+// Every rounding step is written with an explicit _rn intrinsic so that the
+// codes are bit-reproducible: fp32 block sum in token order, IEEE division,
+// round-to-nearest-even conversions (cvt.rn.satfinite.e4m3x2).
+#include <cuda_bf16.h>
+
+#include "vc_device.cuh"
+#include "vc_internal.h"
+
+namespace vc {
+namespace {
+
+constexpr int kQkThreads = 256;
+
+struct QkArgs {
+    const uint16_t* X;
+    int64_t s_b, s_n, s_h;
+    const int32_t* perm;  // may be null
+    uint8_t* X8;
+    float* sx;
+    int H, N, nblk;
+    int64_t Npad;
+};
+
+// One CTA per (block j, head h, batch b, tensor which); 2 threads per token row.
+template <int D>
+__global__ void __launch_bounds__(kQkThreads) quant_qk_kernel(QkArgs q, QkArgs k) {
+    constexpr int CH = D / 2;           // channels per thread
+    constexpr int NV = CH / 8;          // 16-byte vectors per thread
+    const QkArgs& a = (blockIdx.z & 1) ? k : q;
+    const int b = blockIdx.z >> 1, h = blockIdx.y, j = blockIdx.x;
+    const int bh = b * a.H + h;
+    const int row = threadIdx.x >> 1, half = threadIdx.x & 1;
+    const int t = j * kBlock + row;
+    const bool valid = t < a.N;
+
+    float x[CH];
+    float amax = 0.f;
+    if (valid) {
+        const int src = a.perm ? __ldg(a.perm + (int64_t)bh * a.N + t) : t;
+        const uint4* p = reinterpret_cast<const uint4*>(a.X + (int64_t)b * a.s_b + (int64_t)src * a.s_n +
+                                                        (int64_t)h * a.s_h + half * CH);
+#pragma unroll
+        for (int v = 0; v < NV; ++v) {
+            uint4 w = __ldg(p + v);
+            uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                x[v * 8 + 2 * e] = bf16_bits_to_f32(ws[e] & 0xFFFFu);
+                x[v * 8 + 2 * e + 1] = bf16_bits_to_f32(ws[e] >> 16);
+            }
+        }
+#pragma unroll
+        for (int c = 0; c < CH; ++c) amax = fmaxf(amax, fabsf(x[c]));
+    }
+    __shared__ float red[kQkThreads / 32];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+    __syncthreads();
+    amax = red[0];
+#pragma unroll
+    for (int w = 1; w < kQkThreads / 32; ++w) amax = fmaxf(amax, red[w]);
+
+    const float inv = amax > 0.f ? __fdiv_rn(448.f, amax) : 0.f;
+    if (threadIdx.x == 0) a.sx[(int64_t)bh * a.nblk + j] = __fdiv_rn(amax, 448.f);
+
+    uint4* out = reinterpret_cast<uint4*>(a.X8 + ((int64_t)bh * a.Npad + t) * D + half * CH);
+#pragma unroll
+    for (int v = 0; v < CH / 16; ++v) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            if (valid) {
+                const int c = v * 16 + 4 * e;
+                uint32_t lo = cvt_e4m3x2(__fmul_rn(x[c], inv), __fmul_rn(x[c + 1], inv));
+                uint32_t hi = cvt_e4m3x2(__fmul_rn(x[c + 2], inv), __fmul_rn(x[c + 3], inv));
+                w[e] = lo | (hi << 16);
+            } else {
+                w[e] = 0u;
+            }
+        }
+        out[v] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+struct VArgs {
+    const uint16_t* V;
+    int64_t s_b, s_n, s_h;
+    const int32_t* perm;
+    int H, N, nblk;
+    int64_t Npad;
+    int vsmooth;
+    uint16_t* mu;       // [B,H,nblk,D]
+    uint32_t* amax_ws;  // [B,H,D] fp32 bit patterns
+    uint8_t* V8T;       // [B,H,D,Npad]
+    float* sv;          // [B,H,D]
+};
+
+// Loads the block's 128 rows of channel c of V' (gathered) into registers.
+template <int D>
+__device__ __forceinline__ int load_v_column(const VArgs& a, int b, int h, int j, int c, float (&v)[kBlock],
+                                             int32_t* src_s) {
+    const int bh = b * a.H + h;
+    const int t0 = j * kBlock;
+    const int cnt = min(kBlock, a.N - t0);
+    for (int i = threadIdx.x; i < kBlock; i += blockDim.x)
+        src_s[i] = (i < cnt) ? (a.perm ? __ldg(a.perm + (int64_t)bh * a.N + t0 + i) : t0 + i) : 0;
+    __syncthreads();
+    const uint16_t* base = a.V + (int64_t)b * a.s_b + (int64_t)h * a.s_h + c;
+#pragma unroll
+    for (int i = 0; i < kBlock; ++i) {
+        v[i] = (i < cnt) ? bf16_bits_to_f32(__ldg(base + (int64_t)src_s[i] * a.s_n)) : 0.f;
+    }
+    return cnt;
+}
+
+template <int D>
+__global__ void __launch_bounds__(D) quant_v_stats_kernel(VArgs a) {
+    __shared__ int32_t src_s[kBlock];
+    const int b = blockIdx.z, h = blockIdx.y, j = blockIdx.x, c = threadIdx.x;
+    const int bh = b * a.H + h;
+    float v[kBlock];
+    const int cnt = load_v_column<D>(a, b, h, j, c, v, src_s);
+    float m = 0.f;
+    if (a.vsmooth) {
+        float sum = 0.f;
+#pragma unroll
+        for (int i = 0; i < kBlock; ++i)
+            if (i < cnt) sum = __fadd_rn(sum, v[i]);
+        const __nv_bfloat16 mb = __float2bfloat16_rn(__fdiv_rn(sum, (float)cnt));
+        const uint16_t bits = __bfloat16_as_ushort(mb);
+        a.mu[((int64_t)bh * a.nblk + j) * D + c] = bits;
+        m = bf16_bits_to_f32(bits);
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < kBlock; ++i)
+        if (i < cnt) amax = fmaxf(amax, fabsf(__fsub_rn(v[i], m)));
+    atomicMax(a.amax_ws + (int64_t)bh * D + c, __float_as_uint(amax));
+}
+
+template <int D>
+__global__ void __launch_bounds__(D) quant_v_codes_kernel(VArgs a) {
+    __shared__ int32_t src_s[kBlock];
+    const int b = blockIdx.z, h = blockIdx.y, j = blockIdx.x, c = threadIdx.x;
+    const int bh = b * a.H + h;
+    float v[kBlock];
+    const int cnt = load_v_column<D>(a, b, h, j, c, v, src_s);
+    const float m = a.vsmooth ? bf16_bits_to_f32(a.mu[((int64_t)bh * a.nblk + j) * D + c]) : 0.f;
+    const float amax = __uint_as_float(a.amax_ws[(int64_t)bh * D + c]);
+    const float inv = amax > 0.f ? __fdiv_rn(448.f, amax) : 0.f;
+    if (j == 0) a.sv[(int64_t)bh * D + c] = __fdiv_rn(amax, 448.f);
+    uint4* out = reinterpret_cast<uint4*>(a.V8T + ((int64_t)bh * D + c) * a.Npad + (int64_t)j * kBlock);
+#pragma unroll
+    for (int g = 0; g < kBlock / 16; ++g) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int i = g * 16 + 4 * e;
+            float r[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) r[u] = (i + u < cnt) ? __fmul_rn(__fsub_rn(v[i + u], m), inv) : 0.f;
+            w[e] = cvt_e4m3x2(r[0], r[1]) | (cvt_e4m3x2(r[2], r[3]) << 16);
+        }
+        out[g] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+}  // namespace
+
+size_t quantize_workspace(const vc_shape& s) { return (size_t)s.B * s.H * s.d * sizeof(uint32_t); }
+
+template <int D>
+static vc_status launch_quantize_d(const uint16_t* Q, const uint16_t* K, const uint16_t* V, const vc_shape& s,
+                                   const int32_t* perm, int vsmooth, uint8_t* Q8, float* sq, uint8_t* K8,
+                                   float* sk, uint8_t* V8T, float* sv, uint16_t* mu, void* ws, cudaStream_t st) {
+    const int nblk = nblk_of(s.N);
+    const int64_t Npad = npad_of(s.N);
+    QkArgs qa{Q, s.s_b, s.s_n, s.s_h, nullptr, Q8, sq, s.H, s.N, nblk, Npad};
+    QkArgs ka{K, s.s_b, s.s_n, s.s_h, perm, K8, sk, s.H, s.N, nblk, Npad};
+    quant_qk_kernel<D><<<dim3(nblk, s.H, 2 * s.B), kQkThreads, 0, st>>>(qa, ka);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_status(e);
+    uint32_t* amax_ws = static_cast<uint32_t*>(ws);
+    e = cudaMemsetAsync(amax_ws, 0, quantize_workspace(s), st);
+    if (e != cudaSuccess) return cuda_status(e);
+    VArgs va{V, s.s_b, s.s_n, s.s_h, perm, s.H, s.N, nblk, Npad, vsmooth, mu, amax_ws, V8T, sv};
+    quant_v_stats_kernel<D><<<dim3(nblk, s.H, s.B), D, 0, st>>>(va);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_status(e);
+    quant_v_codes_kernel<D><<<dim3(nblk, s.H, s.B), D, 0, st>>>(va);
+    return cuda_status(cudaGetLastError());
+}
+
+vc_status launch_quantize(const uint16_t* Q, const uint16_t* K, const uint16_t* V, const vc_shape& s,
+                          const int32_t* perm, int vsmooth, uint8_t* Q8, float* sq, uint8_t* K8, float* sk,
+                          uint8_t* V8T, float* sv, uint16_t* mu, void* ws, cudaStream_t st) {
+    if (s.d == 128)
+        return launch_quantize_d<128>(Q, K, V, s, perm, vsmooth, Q8, sq, K8, sk, V8T, sv, mu, ws, st);
+    return launch_quantize_d<64>(Q, K, V, s, perm, vsmooth, Q8, sq, K8, sk, V8T, sv, mu, ws, st);
+}
+
+}  // namespace vc

@@ -1,0 +1,203 @@
+"""Thin ctypes binding over libvc_gb300.so (the C ABI in include/vc.h).
+
+Argument marshalling only: every step of the path runs in the library's CUDA
+kernels.  PyTorch supplies device memory and the current stream.  There is no
+fallback: if the library has not been built, every call raises.
+"""
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libvc_gb300.so")
+BLOCK = 128
+
+STATUS = {0: "VC_OK", 1: "VC_ERR_INVALID_ARG", 2: "VC_ERR_UNSUPPORTED", 3: "VC_ERR_WORKSPACE",
+          4: "VC_ERR_CUDA", 5: "VC_ERR_TIMEOUT"}
+
+
+class VcError(RuntimeError):
+    def __init__(self, code, where):
+        super().__init__("%s failed: %s" % (where, STATUS.get(code, code)))
+        self.code = code
+
+
+class VcShape(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("H", ctypes.c_int32), ("N", ctypes.c_int32), ("d", ctypes.c_int32),
+                ("s_b", ctypes.c_int64), ("s_n", ctypes.c_int64), ("s_h", ctypes.c_int64)]
+
+
+_lib = None
+_vp = ctypes.c_void_p
+
+
+def lib():
+    """Load the CUDA library; raises if it was not built (no silent fallback)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("libvc_gb300.so is missing: build it with `python -c \"import __graft_entry__ as g; "
+                               "g.build()\"` (nvcc, sm_103a)")
+        L = ctypes.CDLL(LIB_PATH)
+        L.vc_status_string.restype = ctypes.c_char_p
+        L.vc_status_string.argtypes = [ctypes.c_int]
+        L.vc_version.restype = ctypes.c_int
+        L.vc_cluster_workspace.restype = ctypes.c_size_t
+        L.vc_cluster_workspace.argtypes = [VcShape, ctypes.c_int]
+        L.vc_cluster.restype = ctypes.c_int
+        L.vc_cluster.argtypes = [_vp, VcShape, ctypes.c_int, ctypes.c_int, ctypes.c_int, _vp, _vp, _vp, _vp,
+                                 ctypes.c_size_t, _vp, _vp]
+        L.vc_quantize_workspace.restype = ctypes.c_size_t
+        L.vc_quantize_workspace.argtypes = [VcShape]
+        L.vc_quantize.restype = ctypes.c_int
+        L.vc_quantize.argtypes = [_vp, _vp, _vp, VcShape, _vp, ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                  _vp, ctypes.c_size_t, _vp]
+        L.vc_attn_fwd.restype = ctypes.c_int
+        L.vc_attn_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, VcShape, ctypes.c_float, ctypes.c_int,
+                                  ctypes.c_int, _vp, _vp, _vp]
+        L.vc_attn_fwd_debug.restype = ctypes.c_int
+        L.vc_attn_fwd_debug.argtypes = L.vc_attn_fwd.argtypes + [ctypes.c_int, ctypes.c_int, _vp, _vp]
+        L.vc_debug_e4m3_encode.restype = ctypes.c_int
+        L.vc_debug_e4m3_encode.argtypes = [_vp, ctypes.c_int64, _vp, _vp]
+        L.vc_debug_wait_timeout.restype = ctypes.c_int
+        L.vc_debug_wait_timeout.argtypes = [_vp, ctypes.c_uint32, _vp]
+        _lib = L
+    return _lib
+
+
+def _check(code, where):
+    if code != 0:
+        raise VcError(code, where)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def nblk_of(N):
+    return (N + BLOCK - 1) // BLOCK
+
+
+def shape_of(X: torch.Tensor) -> VcShape:
+    """[B, N, H, d] bf16 tensor with unit channel stride -> vc_shape."""
+    if X.dim() != 4 or X.stride(3) != 1:
+        raise ValueError("expected [B, N, H, d] with unit channel stride")
+    B, N, H, d = X.shape
+    return VcShape(B, H, N, d, X.stride(0), X.stride(1), X.stride(2))
+
+
+def _empty(shape, dtype, device, fill=None):
+    t = torch.empty(shape, dtype=dtype, device=device)
+    if fill is not None:
+        t.fill_(fill)
+    return t
+
+
+def quantize_workspace_bytes(shape: VcShape) -> int:
+    return lib().vc_quantize_workspace(shape)
+
+
+def cluster_workspace_bytes(shape: VcShape, k: int) -> int:
+    return lib().vc_cluster_workspace(shape, k)
+
+
+def _workspace(nbytes, device):
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def vc_cluster(V, k, iters, warm_start=False, centroids=None, labels=None, perm=None, workspace=None,
+               dev_status=None, stream=None):
+    """Grouping step. Returns (centroids fp32 [B,H,k,d], labels int32 [B,H,N], perm int32 [B,H,N])."""
+    s = shape_of(V)
+    dev = V.device
+    if centroids is None:
+        if warm_start:
+            raise ValueError("warm start needs centroids")
+        centroids = _empty((s.B, s.H, k, s.d), torch.float32, dev)
+    if labels is None:
+        labels = _empty((s.B, s.H, s.N), torch.int32, dev)
+    if perm is None:
+        perm = _empty((s.B, s.H, s.N), torch.int32, dev)
+    need = lib().vc_cluster_workspace(s, k)
+    if workspace is None:
+        workspace = _workspace(need, dev)
+    rc = lib().vc_cluster(_ptr(V), s, k, iters, int(bool(warm_start)), _ptr(centroids), _ptr(labels), _ptr(perm),
+                          _ptr(workspace), workspace.numel(), _ptr(dev_status), _stream(stream))
+    _check(rc, "vc_cluster")
+    return centroids, labels, perm
+
+
+def alloc_quantized(shape: VcShape, device, vsmooth=1):
+    nb = nblk_of(shape.N)
+    npad = nb * BLOCK
+    B, H, d = shape.B, shape.H, shape.d
+    return dict(
+        Q8=_empty((B, H, npad, d), torch.uint8, device), sq=_empty((B, H, nb), torch.float32, device),
+        K8=_empty((B, H, npad, d), torch.uint8, device), sk=_empty((B, H, nb), torch.float32, device),
+        V8T=_empty((B, H, d, npad), torch.uint8, device), sv=_empty((B, H, d), torch.float32, device),
+        mu=_empty((B, H, nb, d), torch.int16, device) if vsmooth else None)
+
+
+def vc_quantize(Q, K, V, perm=None, vsmooth=1, out=None, workspace=None, stream=None):
+    """Fused quantizer. Returns a dict with Q8, sq, K8, sk, V8T, sv, mu (mu is bf16 bits as int16)."""
+    s = shape_of(Q)
+    if shape_of(K).N != s.N or shape_of(V).N != s.N:
+        raise ValueError("Q, K, V shapes differ")
+    if (K.stride(), V.stride()) != (Q.stride(), Q.stride()):
+        raise ValueError("Q, K, V must share strides")
+    dev = Q.device
+    if out is None:
+        out = alloc_quantized(s, dev, vsmooth)
+    need = lib().vc_quantize_workspace(s)
+    if workspace is None:
+        workspace = _workspace(need, dev)
+    rc = lib().vc_quantize(_ptr(Q), _ptr(K), _ptr(V), s, _ptr(perm), int(vsmooth), _ptr(out["Q8"]),
+                           _ptr(out["sq"]), _ptr(out["K8"]), _ptr(out["sk"]), _ptr(out["V8T"]), _ptr(out["sv"]),
+                           _ptr(out["mu"]) if vsmooth else None, _ptr(workspace), workspace.numel(),
+                           _stream(stream))
+    _check(rc, "vc_quantize")
+    return out
+
+
+def vc_attn_fwd(qz, shape: VcShape, softmax_scale=0.0, expcast=1, vsmooth=1, O=None, dev_status=None,
+                stream=None, debug=None):
+    """FP8 attention on vc_quantize outputs. O is bf16 [B,N,H,d] laid out with `shape`'s strides.
+
+    debug=(bh, qtile) additionally returns the fp32 scores and probability bytes
+    of that one query tile: (O, S_dump [128, Npad], P_dump [128, Npad]).
+    """
+    dev = qz["Q8"].device
+    if O is None:
+        O = torch.empty((shape.B, shape.N, shape.H, shape.d), dtype=torch.bfloat16, device=dev)
+        if (O.stride(0), O.stride(1), O.stride(2)) != (shape.s_b, shape.s_n, shape.s_h):
+            O = torch.empty_strided((shape.B, shape.N, shape.H, shape.d), (shape.s_b, shape.s_n, shape.s_h, 1),
+                                    dtype=torch.bfloat16, device=dev)
+    args = [_ptr(qz["Q8"]), _ptr(qz["sq"]), _ptr(qz["K8"]), _ptr(qz["sk"]), _ptr(qz["V8T"]), _ptr(qz["sv"]),
+            _ptr(qz["mu"]) if vsmooth else None, shape, float(softmax_scale), int(expcast), int(vsmooth), _ptr(O),
+            _ptr(dev_status), _stream(stream)]
+    if debug is None:
+        _check(lib().vc_attn_fwd(*args), "vc_attn_fwd")
+        return O
+    npad = nblk_of(shape.N) * BLOCK
+    S = torch.zeros((BLOCK, npad), dtype=torch.float32, device=dev)
+    P = torch.zeros((BLOCK, npad), dtype=torch.uint8, device=dev)
+    _check(lib().vc_attn_fwd_debug(*args, int(debug[0]), int(debug[1]), _ptr(S), _ptr(P)), "vc_attn_fwd_debug")
+    return O, S, P
+
+
+def vc_debug_e4m3_encode(x: torch.Tensor, out=None, stream=None):
+    if out is None:
+        out = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    _check(lib().vc_debug_e4m3_encode(_ptr(x), x.numel(), _ptr(out), _stream(stream)), "vc_debug_e4m3_encode")
+    return out
+
+
+def vc_debug_wait_timeout(dev_status: torch.Tensor, timeout_us: int, stream=None):
+    _check(lib().vc_debug_wait_timeout(_ptr(dev_status), int(timeout_us), _stream(stream)), "vc_debug_wait_timeout")

@@ -1,0 +1,195 @@
+/*
+ * vc.h -- C ABI of the VC-Attention hot path for one GB300 (sm_103a).
+ *
+ * Non-causal attention O = softmax(Q K^T * scale) V computed in FP8 with the
+ * two techniques of "VC-Attention: Value Smoothing and Softmax Casting for
+ * Low-bit Attention":
+ *   V-Smooth  -- value tokens of each (batch, head) are grouped by online
+ *                k-means, K and V are gathered jointly into cluster order
+ *                (exact for non-causal attention, P'V' = PV), every 128-token
+ *                block mean mu_j is kept in 16 bits and only the residual is
+ *                quantized to E4M3 with per-channel scales; the mean is added
+ *                back inside the online softmax from the row sums r_ij.
+ *   ExpCast   -- each E4M3 probability byte is written from the log-domain
+ *                score by one FMA: c = clip(Round(8(u+8) + 56 + beta), 0, 120),
+ *                beta = -0.35, replacing the FP32 exp and the cast.
+ * Passages: paper summary on paper.rainbus.top (方法步骤详情, steps 1-4;
+ * 前置知识 "在线 softmax", "E4M3 浮点格式"); study note on
+ * dimensionstp.github.io (sections 2-1 .. 2-4); wire.sakhanda.co article
+ * (sections "V-Smooth", "ExpCast-FP8").
+ *
+ * Conventions shared by every entry point
+ *   - Every pointer is device memory owned by the caller unless stated.  The
+ *     library never allocates or frees memory and keeps no per-call state;
+ *     calls on different streams with disjoint buffers may run concurrently.
+ *   - All work is enqueued asynchronously on `stream` (NULL = legacy default
+ *     stream).  A return of VC_OK means the launches were enqueued.
+ *   - Argument and shape errors are detected on the host before anything is
+ *     launched and return VC_ERR_INVALID_ARG / VC_ERR_UNSUPPORTED /
+ *     VC_ERR_WORKSPACE.  A failed launch returns VC_ERR_CUDA.
+ *   - Every wait inside a kernel is bounded.  A wait that runs out writes
+ *     VC_ERR_TIMEOUT to *dev_status (an int32 in device memory, nullable;
+ *     the caller zeroes it beforehand and reads it after synchronising); the
+ *     kernel then releases what it holds and returns instead of hanging.
+ *   - Token blocks are 128 tokens; nblk = ceil(N/128), Npad = 128*nblk.
+ *   - NaN or Inf inputs are outside the contract.
+ */
+#ifndef VC_H_
+#define VC_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ABI-identical to cudaStream_t; declared here so this header needs no CUDA headers. */
+typedef struct CUstream_st* vc_stream_t;
+
+typedef enum {
+    VC_OK = 0,
+    VC_ERR_INVALID_ARG = 1, /* null pointer, non-positive size, bad stride, bad flag */
+    VC_ERR_UNSUPPORTED = 2, /* d not in {64, 128}, k outside [1, 1024], N > 2^24 */
+    VC_ERR_WORKSPACE = 3,   /* workspace pointer null or smaller than the query says */
+    VC_ERR_CUDA = 4,        /* a CUDA launch or driver call failed */
+    VC_ERR_TIMEOUT = 5      /* a bounded device wait ran out (written to *dev_status) */
+} vc_status;
+
+/*
+ * Shape and strides of a bf16 tensor laid out [B, N, H, d] (channel stride 1).
+ * Strides are in elements; the usual contiguous layout has
+ * s_b = N*H*d, s_n = H*d, s_h = d.  Every stride must be a multiple of 8
+ * (16-byte rows) and every bf16 base pointer 16-byte aligned.
+ */
+typedef struct {
+    int32_t B, H, N, d;
+    int64_t s_b, s_n, s_h;
+} vc_shape;
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char* vc_status_string(vc_status s);
+
+/* Library ABI version (major*100 + minor). */
+int vc_version(void);
+
+/*
+ * Grouping step, paper summary 方法步骤详情 step 1 (online k-means on the value
+ * tokens of each batch/head, pi = argsort(z)); dimensionstp.github.io 2-1.
+ *
+ *   V          bf16 [B,N,H,d] with `shape` strides (read only).
+ *   k          number of centroids, 1 <= k <= 1024, k <= N.
+ *   iters      Lloyd iterations, >= 1.  Each iteration assigns every token to
+ *              its nearest centroid (squared Euclidean distance) and moves each
+ *              centroid to the mean of its members; an empty cluster keeps its
+ *              centroid.
+ *   warm_start 1: start from `centroids` as given (previous step's state);
+ *              0: centroid i starts at token floor(i*N/k).
+ *   centroids  fp32 [B,H,k,d], in/out (the warm-start state the caller keeps).
+ *   labels     int32 [B,H,N], out: label of every token from the last
+ *              assignment (the centroids are the means of these groups).
+ *   perm       int32 [B,H,N], out: pi, the stable argsort of labels (ascending
+ *              label, equal labels in token order).  Row t of K' and V' is
+ *              token perm[t].
+ *   workspace  device scratch of at least vc_cluster_workspace(shape, k) bytes,
+ *              256-byte aligned; contents on entry are ignored.
+ * Label choice between near-equidistant centroids follows fp32 rounding and
+ * is not guaranteed to be bit-reproducible across hardware.
+ */
+size_t vc_cluster_workspace(vc_shape shape, int k);
+vc_status vc_cluster(const void* V, vc_shape shape, int k, int iters, int warm_start,
+                     float* centroids, int32_t* labels, int32_t* perm,
+                     void* workspace, size_t workspace_bytes,
+                     int32_t* dev_status, vc_stream_t stream);
+
+/*
+ * Fused quantizer, paper summary 方法步骤详情 step 2 and 前置知识 "低比特量化与
+ * 离群值"; dimensionstp.github.io 2-2 (mu_j = (1/B_v) V'_j^T 1, R_j = V'_j - 1 mu_j^T).
+ *
+ *   Q, K, V    bf16 [B,N,H,d] with `shape` strides (read only).
+ *   perm       int32 [B,H,N] or NULL (identity).  K' = K[perm], V' = V[perm]
+ *              (the joint gather); Q keeps its order.
+ *   vsmooth    1: subtract each 128-token block mean of V' (kept as bf16 in
+ *              `mu`) and quantize the residual; 0: quantize V' directly
+ *              (`mu` may be NULL and is not written).
+ *   Q8, K8     E4M3 [B,H,Npad,d]: code = E4M3_RNE_sat(x * (448/amax)), one
+ *              scale per 128-token block; rows >= N are written as 0.
+ *   sq, sk     fp32 [B,H,nblk]: amax/448 of each block (0 for an all-zero block).
+ *   V8T        E4M3 [B,H,d,Npad] (token-contiguous per channel): residual
+ *              codes with one scale per channel over the whole sequence;
+ *              tokens >= N are 0.
+ *   sv         fp32 [B,H,d]: per-channel scale amax_t|R[t,c]|/448.
+ *   mu         bf16 [B,H,nblk,d]: bf16_RNE(fp32 sum in token order / count).
+ *   workspace  >= vc_quantize_workspace(shape) bytes, 256-byte aligned.
+ * Output pointers must be 16-byte aligned.  Codes and scales are
+ * deterministic and bit-reproducible.
+ */
+size_t vc_quantize_workspace(vc_shape shape);
+vc_status vc_quantize(const void* Q, const void* K, const void* V, vc_shape shape,
+                      const int32_t* perm, int vsmooth,
+                      uint8_t* Q8, float* sq, uint8_t* K8, float* sk,
+                      uint8_t* V8T, float* sv, void* mu,
+                      void* workspace, size_t workspace_bytes, vc_stream_t stream);
+
+/*
+ * FP8 attention forward, paper summary 前置知识 "在线 softmax" and 方法步骤详情
+ * steps 3-4; dimensionstp.github.io 2-3 (P_ij V'_j = P_ij R_j + r_ij mu_j^T)
+ * and 2-4.  Takes the outputs of vc_quantize.
+ *
+ * For each query row i, keys are visited in 128-token tiles in stored order
+ * with an exact running max m' (scores in log2 units):
+ *   acc    = sum_c q8*k8 (tcgen05 FP8 MMA, fp32 accumulate)
+ *   sigma  = fp32(fp32(sq_i*sk_j) * kscale), kscale = fp32(scale * log2 e)
+ *   m'     = max(m, sigma * max_k acc)
+ *   expcast=1: c = clamp(rint(fmaf(acc, 8 sigma, fmaf(-8, m', 119.65f))), 0, 120)
+ *   expcast=0: c = E4M3_RNE_sat(exp2(fmaf(acc, sigma, 8 - m')))
+ *   r_ij   = sum_k decode(c)            (row sum of the quantized P)
+ *   l     <- alpha l + r_ij,  alpha = exp2(m - m')
+ *   A     <- alpha A + P_q V8_res * s_v + r_ij mu_j   (mu term only if vsmooth)
+ *   O      = A / l, stored as bf16.
+ *
+ *   softmax_scale  > 0, or <= 0 for 1/sqrt(d).
+ *   O        bf16 [B,N,H,d] with `shape` strides (rows in original query order).
+ *   dev_status  nullable; receives VC_ERR_TIMEOUT if a device wait ran out.
+ * Q8/K8/V8T must be 16-byte aligned (they are read with TMA).
+ */
+vc_status vc_attn_fwd(const uint8_t* Q8, const float* sq, const uint8_t* K8, const float* sk,
+                      const uint8_t* V8T, const float* sv, const void* mu, vc_shape shape,
+                      float softmax_scale, int expcast, int vsmooth,
+                      void* O, int32_t* dev_status, vc_stream_t stream);
+
+/*
+ * Test hook for the ExpCast byte check: runs vc_attn_fwd and additionally,
+ * for the single query tile `dbg_qtile` of head-slot `dbg_bh` (= b*H + h),
+ * writes the fp32 scores acc it computed, S_dump fp32 [128, Npad], and the
+ * probability bytes it fed to the PV product, P_dump uint8 [128, Npad]
+ * (rows = the tile's 128 query rows, columns = keys in stored order).
+ * Same contract as vc_attn_fwd otherwise; slower (a separate instantiation).
+ */
+vc_status vc_attn_fwd_debug(const uint8_t* Q8, const float* sq, const uint8_t* K8, const float* sk,
+                            const uint8_t* V8T, const float* sv, const void* mu, vc_shape shape,
+                            float softmax_scale, int expcast, int vsmooth,
+                            void* O, int32_t* dev_status, vc_stream_t stream,
+                            int dbg_bh, int dbg_qtile, float* S_dump, uint8_t* P_dump);
+
+/*
+ * Test hook: the device conversion the quantizer uses to write E4M3 codes
+ * (round to nearest even, saturating to +-448), applied to n fp32 values.
+ * x: fp32 [n], out: uint8 [n], both device memory.  Lets tests compare the
+ * hardware conversion with an independent encoder over all fp32 patterns.
+ */
+vc_status vc_debug_e4m3_encode(const float* x, int64_t n, uint8_t* out, vc_stream_t stream);
+
+/*
+ * Test hook: launches one CTA whose mbarrier wait can never complete (two
+ * arrivals expected, one made).  The library's bounded wait gives up after
+ * timeout_us microseconds (1 .. 10^7), writes VC_ERR_TIMEOUT to *dev_status
+ * and the kernel returns; the CUDA context stays usable.
+ */
+vc_status vc_debug_wait_timeout(int32_t* dev_status, uint32_t timeout_us, vc_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VC_H_ */

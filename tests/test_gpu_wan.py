@@ -1,0 +1,56 @@
+"""Full-size parity on the Wan2.2-shaped workload (B=1, H=40, N=75,600, d=128).
+
+The whole path runs at full size in the launch configuration the benchmark
+times; the oracle checks what it can compute one by one: the quantizer
+bit-exactly for two heads, O on sampled query rows of those heads (including
+the ragged last tile), and the grouping invariants on sampled tokens.
+"""
+import numpy as np
+import pytest
+import torch
+
+from bit_fp8_attention_means_gb300 import inputs, vc
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+u16 = inputs.to_u16
+
+
+def test_wan_full_size_sampled(oracle_mod):
+    w = inputs.WORKLOADS["wan"]
+    Q, K, V = inputs.make_qkv(w, DEV)
+    cent, _, _ = vc.vc_cluster(V, w.k, w.iters)
+    c_prev = cent.clone()
+    cent, lab, perm = vc.vc_cluster(V, w.k, 1, warm_start=True, centroids=cent)
+    qz = vc.vc_quantize(Q, K, V, perm, 1)
+    O = vc.vc_attn_fwd(qz, vc.shape_of(Q), expcast=1, vsmooth=1)
+    torch.cuda.synchronize()
+    N = w.N
+    nb = vc.nblk_of(N)
+    rng = np.random.default_rng(0)
+    for h in (0, 23, 39):
+        Qh, Kh, Vh = (u16(t[:, :, h:h + 1]) for t in (Q, K, V))
+        ph = perm[:, h:h + 1].cpu().numpy()
+        lh = lab[:, h:h + 1].cpu().numpy()
+        # pi is the stable argsort of the labels
+        np.testing.assert_array_equal(ph[0, 0], np.argsort(lh[0, 0], kind="stable"))
+        # labels are nearest centroids on sampled tokens
+        v = oracle_mod.bf16_to_f32(Vh).astype(np.float64)[0, :, 0]
+        cp = c_prev[0, h].cpu().numpy().astype(np.float64)
+        toks = rng.choice(N, 512, replace=False)
+        d2 = ((v[toks][:, None] - cp[None]) ** 2).sum(-1)
+        chosen = d2[np.arange(toks.size), lh[0, 0, toks]]
+        scale = (v[toks] ** 2).sum(-1) + (cp ** 2).sum(-1)[lh[0, 0, toks]]
+        assert np.all(chosen - d2.min(1) <= 4 * 128 * 2.0 ** -24 * scale + 1e-6)
+        # quantizer bit-exact for this head
+        want = oracle_mod.quantize(Qh, Kh, Vh, ph, 1)
+        for key in ("Q8", "sq", "K8", "sk", "V8T", "sv"):
+            np.testing.assert_array_equal(qz[key][:, h:h + 1].cpu().numpy(), want[key], err_msg=key)
+        np.testing.assert_array_equal(qz["mu"][:, h:h + 1].cpu().numpy().view(np.uint16), want["mu"])
+        # O on sampled rows, including the last (80-row) tile
+        rows = np.unique(np.concatenate([rng.choice(N, 40, replace=False), np.arange(N - 8, N),
+                                         np.arange((nb - 1) * 128, (nb - 1) * 128 + 4)])).astype(np.int32)
+        ref = oracle_mod.attn(want, N, rows=rows)[0, 0]
+        got = O[0, rows, h].float().cpu().numpy()
+        rel = np.linalg.norm(got - ref) / np.linalg.norm(ref)
+        assert rel <= 2e-3, (h, rel)

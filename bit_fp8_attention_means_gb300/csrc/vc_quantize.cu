@@ -215,3 +215,67 @@ vc_status launch_quantize(const uint16_t* Q, const uint16_t* K, const uint16_t* 
 }
 
 }  // namespace vc
+
+// ------------------------------------------------------------------ fixed-scratch variant
+//
+// vc_quantize needs B*H*d words of device scratch for the per-channel residual
+// maxima.  Some callers cannot hand it any: a host that embeds this library
+// inside a framework whose memory pool owns all device memory (a raw
+// cudaMalloc would bypass its accounting), or code that runs where an
+// allocation would synchronize the device or is simply not permitted.  For
+// them vc_quantize_static keeps that scratch in a fixed array inside this
+// library instead.
+#include <mutex>
+
+namespace vc {
+namespace {
+
+constexpr size_t kStaticScratchWords = 65536;  // B*H*d <= 65536 (256 KB, held by every GPU that loads the library)
+__device__ __align__(256) uint32_t g_quantize_scratch[kStaticScratchWords];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mutex;
+void* g_scratch_addr[kMaxDevices] = {};
+
+// Device address of g_quantize_scratch on the current device; looked up once
+// per device (the host-side name is only a stand-in, never a device pointer).
+vc_status static_scratch(void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return VC_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    if (!g_scratch_addr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_quantize_scratch) != cudaSuccess || !p) return VC_ERR_CUDA;
+        g_scratch_addr[dev] = p;
+    }
+    *out = g_scratch_addr[dev];
+    return VC_OK;
+}
+
+bool aligned16_q(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+}  // namespace vc
+
+extern "C" vc_status vc_quantize_static(const void* Q, const void* K, const void* V, vc_shape shape,
+                                        const int32_t* perm, int vsmooth, uint8_t* Q8, float* sq, uint8_t* K8,
+                                        float* sk, uint8_t* V8T, float* sv, void* mu, vc_stream_t stream) {
+    using namespace vc;
+    vc_status st = check_shape(shape);
+    if (st != VC_OK) return st;
+    if (vsmooth != 0 && vsmooth != 1) return VC_ERR_INVALID_ARG;
+    if (!Q || !K || !V || !Q8 || !sq || !K8 || !sk || !V8T || !sv || (vsmooth && !mu)) return VC_ERR_INVALID_ARG;
+    if (!aligned16_q(Q) || !aligned16_q(K) || !aligned16_q(V) || !aligned16_q(Q8) || !aligned16_q(K8) ||
+        !aligned16_q(V8T))
+        return VC_ERR_INVALID_ARG;
+    if ((size_t)shape.B * shape.H * shape.d > kStaticScratchWords) return VC_ERR_WORKSPACE;
+    void* scratch = nullptr;
+    st = static_scratch(&scratch);
+    if (st != VC_OK) return st;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    const uint16_t *q = static_cast<const uint16_t*>(Q), *k = static_cast<const uint16_t*>(K),
+                   *v = static_cast<const uint16_t*>(V);
+    uint16_t* m = static_cast<uint16_t*>(mu);
+    if (shape.d == 128) return launch_quantize_d<128>(q, k, v, shape, perm, vsmooth, Q8, sq, K8, sk, V8T, sv, m, scratch, cs);
+    return launch_quantize_d<64>(q, k, v, shape, perm, vsmooth, Q8, sq, K8, sk, V8T, sv, m, scratch, cs);
+}

@@ -132,6 +132,33 @@ vc_status vc_quantize(const void* Q, const void* K, const void* V, vc_shape shap
                       void* workspace, size_t workspace_bytes, vc_stream_t stream);
 
 /*
+ * vc_quantize without a workspace argument, for callers that cannot allocate
+ * device memory: a host that embeds this library inside a framework whose
+ * memory pool owns all device memory, or code running where an allocation
+ * would synchronize the device or is not allowed.  (The paper has no
+ * counterpart; this is a deployment convenience of this library.)
+ *
+ * Same arguments, outputs and results as vc_quantize (bit-identical codes,
+ * scales and means).  The per-channel scratch lives in a fixed array compiled
+ * into the library: 65536 32-bit words (256 KB), which every GPU that loads
+ * the library holds until the process exits.  Limit: B*H*d <= 65536 (for
+ * example H <= 512 heads at d = 128 with B = 1); larger shapes return
+ * VC_ERR_WORKSPACE without launching.  Nothing is allocated: no cudaMalloc,
+ * no cudaFree, no allocating library routine.
+ *
+ * The first call on each device looks up the array's device address (with
+ * that device current) and caches it; make that first call before any stream
+ * capture begins.  Every call shares the one array and clears what it needs
+ * at its start, so calls whose work overlaps on the GPU (different streams,
+ * or different host threads on one device) race and must be serialized by
+ * the caller.
+ */
+vc_status vc_quantize_static(const void* Q, const void* K, const void* V, vc_shape shape,
+                             const int32_t* perm, int vsmooth,
+                             uint8_t* Q8, float* sq, uint8_t* K8, float* sk,
+                             uint8_t* V8T, float* sv, void* mu, vc_stream_t stream);
+
+/*
  * FP8 attention forward, paper summary 前置知识 "在线 softmax" and 方法步骤详情
  * steps 3-4; dimensionstp.github.io 2-3 (P_ij V'_j = P_ij R_j + r_ij mu_j^T)
  * and 2-4.  Takes the outputs of vc_quantize.

@@ -8,33 +8,37 @@
 // c = clip(Round(8(u+8)+56+beta), 0, 120)); dimensionstp.github.io 2-3 / 2-4.
 //
 // One CTA = 128 query rows of one (b, h); 10 warps:
-//   warps 0-7  softmax: two warpgroups; thread (wg, row) owns query row `row`
-//              and key columns [64 wg, 64 wg + 64) of each 128-key tile, and
-//              output channels [wg d/2, (wg+1) d/2).  The two halves of a row
-//              exchange their partial maxima through shared memory.
-//   warp 8     producer: TMA loads of Q (once), K and V^T tiles (ring of NS
-//              stages), and the block means mu_j converted to fp32.
+//   warps 0-7  softmax: two warpgroups; thread (wg, row) owns query row `row`,
+//              key columns [64 wg, 64 wg + 64) of each 128-key tile and output
+//              channels [wg d/2, (wg+1) d/2).  The halves of a row exchange
+//              partial maxima through shared memory.
+//   warp 8     producer: TMA loads of Q (once) and of the K and V^T tiles
+//              (ring of NS stages); per tile it also writes the key scale and
+//              the block mean, split into bf16 hi/lo parts, into shared memory.
 //   warp 9     MMA issuer (one thread) and TMEM owner.
 // Tensor memory (512 columns):
-//   S0, S1 [0,256)     fp32 scores of tiles j (double-buffered), QK^T.
-//   P      inside S    the probability bytes of tile j overwrite the first 16
-//                      columns of each half of the score buffer they came from.
-//   O      [256,256+d) fp32 residual accumulator A_res (units of codes).
-//   R      16 columns  r_ij = P_j * 1 from a small MMA against a ones operand.
-// Per key tile j the MMA thread issues QK(j+1) before PV(j), so the tensor
-// core computes the next scores while the softmax warps turn tile j into bytes.
-//
-// The mean term is kept in registers: M <- alpha (M + r_{j-1} mu_{j-1}), applied
-// lazily one tile late, when r_{j-1} has come back from the row-sum MMA; O in
-// TMEM is rescaled only when some row of the warp raised its maximum.  Final
-// output O = (s_v (.) A_res + M) / l.
+//   S0, S1  [0,256)        fp32 scores of key tile j (double-buffered), QK^T.
+//   P       inside S       probability bytes of tile j overwrite the first 16
+//                          columns of each half of the score buffer.
+//   O       [256, 256+d)   fp32 accumulator in residual-code units.
+//   R       16 columns     row sums r_ij of the last 16 tiles: tile j adds
+//                          P_j * e_(j mod 16) into column j mod 16 (one small
+//                          MMA against a ones operand with a single 1-row).
+//   AM      24 columns     bf16 A operand of the batched mean restore.
+// Mean restore, batched: every 16 tiles the softmax warps read the 16 row
+// sums, rescale each to the current running max, split them into bf16 hi/lo
+// parts and the MMA thread adds sum_t r_t mu_t^T to O with one bf16 MMA of
+// depth 48 (terms r_hi mu_hi + r_lo mu_hi + r_hi mu_lo per tile).  The means
+// enter in units of the channel's residual scale g_c (g_c = s_v[c], or 1 for a
+// channel whose residual is identically 0), so O = g (.) A / l at the end.
+// The normaliser l is kept in registers, updated from the same row sums.
 //
 // ExpCast inner loop, per score: ts = sat(acc * sigma/16 + C/128) (one FFMA
 // with saturation = clip to [0, 128] of t/128, exact because /128 and /16 are
 // powers of two), then b = ts*128 + 1.5*2^23 (packed FFMA2) whose low byte is
-// rint(t), then byte packing with PRMT.  The upper clip at 120 is implied
-// while |m'| < 2^19 (t <= 119.65 + 2^-1); rows beyond take a path with an
-// explicit min.
+// rint(t); two integer multiply-adds and one byte permute pack four codes.
+// The upper clip at 120 is implied while |m'| < 2^19 (t <= 119.65 + 2^-1);
+// rows beyond take a path with an explicit min.
 #include <cstdio>
 
 #include <cuda_bf16.h>
@@ -50,6 +54,8 @@ constexpr int kThreads = 320;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr uint32_t kTmemCols = 512;
+constexpr int kBatch = 16;             // key tiles per batched mean restore
+constexpr int kMeanK = 3 * kBatch;     // bf16 depth of the mean MMA
 constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23: adding it rounds to an integer in the low mantissa bits
 
 template <int D>
@@ -60,33 +66,39 @@ struct Cfg {
     static constexpr int VB = D * 128;
     static constexpr uint32_t QK_SWZ = (D == 128) ? kSwizzle128B : kSwizzle64B;
     static constexpr uint32_t QK_SBO = 8 * D;  // bytes per group of 8 rows
+    static constexpr int BM_ROW_GROUP = 6 * 128;        // 8 rows x 48 bf16, stored as 6 core matrices
+    static constexpr int BMB = (D / 8) * BM_ROW_GROUP;  // one mean-operand buffer
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_K = OFF_Q + QB;
     static constexpr int OFF_V = OFF_K + NS * KB;
-    static constexpr int OFF_ONES = OFF_V + NS * VB;
-    static constexpr int OFF_MU = OFF_ONES + 2048;
-    static constexpr int OFF_XCH = OFF_MU + NS * D * 4;
+    static constexpr int OFF_ONES = OFF_V + NS * VB;     // kBatch ones operands of 16 x 128 bytes
+    static constexpr int OFF_BM = OFF_ONES + kBatch * 2048;
+    static constexpr int OFF_SK = OFF_BM + 2 * BMB;
+    static constexpr int OFF_MT = OFF_SK + NS * 16;      // running max per (wg, slot, row)
+    static constexpr int OFF_XCH = OFF_MT + 2 * kBatch * 128 * 4;
     static constexpr int OFF_BAR = OFF_XCH + 2 * 2 * 128 * 4;
     static constexpr int NBAR = 32;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int USED = OFF_MISC + 64;
     // at least 116 KB so that exactly one CTA (and one 512-column TMEM owner) sits on an SM
     static constexpr int SMEM = ((USED > 118784) ? USED : 118784) + 1024;
+    static_assert(SMEM <= 232448, "shared memory budget");
     // barrier indices
     static constexpr int B_Q = 0;
     static constexpr int B_KVF = 1;
     static constexpr int B_KVE = B_KVF + NS;
-    static constexpr int B_MUE = B_KVE + NS;
-    static constexpr int B_SF = B_MUE + NS;
+    static constexpr int B_SF = B_KVE + NS;
     static constexpr int B_PF = B_SF + 2;
     static constexpr int B_OD = B_PF + 2;
     static constexpr int B_XCH = B_OD + 1;
-    static constexpr int B_TD = B_XCH + 2;
+    static constexpr int B_PL = B_XCH + 2;
+    static constexpr int B_OF = B_PL + 1;
+    static constexpr int B_TD = B_OF + 1;
     static constexpr int NBAR_USED = B_TD + 1;
     static_assert(NBAR_USED <= NBAR, "barrier area");
     // TMEM columns
-    static constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O = 256, COL_R = 256 + D;
-    static_assert(COL_R + 16 <= kTmemCols, "tmem budget");
+    static constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O = 256, COL_R = 256 + D, COL_AM = 256 + D + 16;
+    static_assert(COL_AM + kMeanK / 2 <= kTmemCols, "tmem budget");
 };
 
 struct AttnParams {
@@ -123,6 +135,14 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64
     }
 }
 
+// Byte offset of element (n, k) of a mean operand buffer: K-major, no swizzle,
+// core matrices of 8 rows x 8 bf16 (16 bytes), 6 along K per group of 8 rows.
+__device__ __forceinline__ uint32_t bm_offset(int n, int k) {
+    return (uint32_t)((n >> 3) * (6 * 128) + (k >> 3) * 128 + (n & 7) * 16 + (k & 7) * 2);
+}
+
+__device__ __forceinline__ uint16_t bf16_rn_bits(float x) { return __bfloat16_as_ushort(__float2bfloat16_rn(x)); }
+
 template <int D, bool EXPCAST, bool VSMOOTH, bool DBG>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -148,7 +168,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < NS; ++s) {
             mbar_init(bar(C::B_KVF + s), 1);
             mbar_init(bar(C::B_KVE + s), 1);
-            mbar_init(bar(C::B_MUE + s), 8);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar(C::B_SF + i), 1);
@@ -156,6 +175,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(C::B_XCH + i), 256);
         }
         mbar_init(bar(C::B_OD), 1);
+        mbar_init(bar(C::B_PL), 8);
+        mbar_init(bar(C::B_OF), 1);
         mbar_init(bar(C::B_TD), 1);
         *abort_flag = 0;
         fence_barrier_init();
@@ -164,10 +185,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_alloc(smem_u32(tmem_slot), kTmemCols);
         tmem_relinquish();
     }
-    if (threadIdx.x < 256) {
-        // ones operand for the row-sum MMA: row 0 = E4M3 1.0 (0x38), rows 1..15 = 0
-        const uint64_t v = (threadIdx.x < 16) ? 0x3838383838383838ull : 0ull;
-        *reinterpret_cast<uint64_t*>(smem + C::OFF_ONES + threadIdx.x * 8) = v;
+    {
+        // Ones operands for the row-sum MMA: operand s has row s = E4M3 1.0 (0x38),
+        // all other rows 0, so P_j * operand (j mod 16) adds r_j to column j mod 16.
+        // A 128-byte row is the same under the 128-byte swizzle, so no swizzle
+        // bookkeeping is needed.  The mean operand buffers start zeroed.
+        uint64_t* ones = reinterpret_cast<uint64_t*>(smem + C::OFF_ONES);
+        for (int i = threadIdx.x; i < kBatch * 2048 / 8; i += kThreads) {
+            const int tile = i / 256, row = (i % 256) / 16;
+            ones[i] = (row == tile) ? 0x3838383838383838ull : 0ull;
+        }
+        uint4* bm = reinterpret_cast<uint4*>(smem + C::OFF_BM);
+        for (int i = threadIdx.x; i < 2 * C::BMB / 16; i += kThreads) bm[i] = make_uint4(0, 0, 0, 0);
         fence_proxy_async_smem();
     }
     tc_fence_before();
@@ -178,6 +207,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kProducerWarp) {
         // ------------------------------------------------------------ producer
         const int32_t row0 = (int32_t)((int64_t)bh * p.Npad);
+        constexpr int PER = D / 32;  // channels per lane for the mean operand
+        float g_ch[PER];
+#pragma unroll
+        for (int e = 0; e < PER; ++e) {
+            const float sv = __ldg(p.sv + (int64_t)bh * D + lane * PER + e);
+            g_ch[e] = sv > 0.f ? sv : 1.f;
+        }
         if (lane == 0) {
             prefetch_tensormap(&tmQ);
             prefetch_tensormap(&tmK);
@@ -189,29 +225,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         int issued = 0;
         for (int j = 0; j < J; ++j) {
             const int s = j % NS, n = j / NS;
-            if (j >= NS) {
-                if (!mbar_wait(bar(C::B_KVE + s), (n - 1) & 1, abort_flag, p.dev_status, tmo)) break;
-                if (VSMOOTH && !mbar_wait(bar(C::B_MUE + s), (n - 1) & 1, abort_flag, p.dev_status, tmo)) break;
-            }
+            if (j >= NS && !mbar_wait(bar(C::B_KVE + s), (n - 1) & 1, abort_flag, p.dev_status, tmo)) break;
             if (lane == 0) {
                 mbar_expect_tx(bar(C::B_KVF + s), C::KB + C::VB);
                 tma_load_2d(sbase + C::OFF_K + s * C::KB, &tmK, 0, row0 + j * 128, bar(C::B_KVF + s));
                 tma_load_2d(sbase + C::OFF_V + s * C::VB, &tmV, j * 128, bh * D, bar(C::B_KVF + s));
+                *reinterpret_cast<float*>(smem + C::OFF_SK + s * 16) = __ldg(p.sk + (int64_t)bh * p.nblk + j);
             }
             if (VSMOOTH) {
-                constexpr int PER = D / 32;
+                // mean operand rows: k = 3t, 3t+1, 3t+2 hold (mu'_hi, mu'_hi, mu'_lo), mu' = mu / g
+                uint8_t* bmb = smem + C::OFF_BM + ((j / kBatch) & 1) * C::BMB;
+                const int k0 = 3 * (j % kBatch);
                 const uint16_t* src = p.mu + ((int64_t)bh * p.nblk + j) * D + lane * PER;
-                float* dst = reinterpret_cast<float*>(smem + C::OFF_MU + s * D * 4) + lane * PER;
-                if (PER == 4) {
-                    const uint2 w = __ldg(reinterpret_cast<const uint2*>(src));
-                    *reinterpret_cast<float4*>(dst) =
-                        make_float4(bf16_bits_to_f32(w.x & 0xFFFFu), bf16_bits_to_f32(w.x >> 16),
-                                    bf16_bits_to_f32(w.y & 0xFFFFu), bf16_bits_to_f32(w.y >> 16));
-                } else {
-                    const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(src));
-                    *reinterpret_cast<float2*>(dst) =
-                        make_float2(bf16_bits_to_f32(w & 0xFFFFu), bf16_bits_to_f32(w >> 16));
+#pragma unroll
+                for (int e = 0; e < PER; ++e) {
+                    const int n_ch = lane * PER + e;
+                    const float mp = __fdiv_rn(bf16_bits_to_f32(__ldg(src + e)), g_ch[e]);
+                    const uint16_t hi = bf16_rn_bits(mp);
+                    const uint16_t lo = bf16_rn_bits(__fsub_rn(mp, bf16_bits_to_f32(hi)));
+                    *reinterpret_cast<uint16_t*>(bmb + bm_offset(n_ch, k0)) = hi;
+                    *reinterpret_cast<uint16_t*>(bmb + bm_offset(n_ch, k0 + 1)) = hi;
+                    *reinterpret_cast<uint16_t*>(bmb + bm_offset(n_ch, k0 + 2)) = lo;
                 }
+                fence_proxy_async_smem();
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(C::B_KVF + s));
@@ -227,6 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t IDESC_QK = idesc_f8_e4m3(128, 128);
             constexpr uint32_t IDESC_PV = idesc_f8_e4m3(128, D);
             constexpr uint32_t IDESC_RS = idesc_f8_e4m3(128, 16);
+            constexpr uint32_t IDESC_MEAN = idesc_bf16(128, D);
             auto issue_qk = [&](int j) {
                 const int s = j % NS;
                 const uint32_t d = tmem + ((j & 1) ? C::COL_S1 : C::COL_S0);
@@ -240,6 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto issue_pv_rs = [&](int j) {
                 const int s = j % NS;
                 const uint32_t pbase = tmem + ((j & 1) ? C::COL_S1 : C::COL_S0);
+                const int slot = j % kBatch;
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
                     const uint32_t a = pbase + (kk < 2 ? kk * 8 : 64 + (kk - 2) * 8);
@@ -249,8 +287,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
                     const uint32_t a = pbase + (kk < 2 ? kk * 8 : 64 + (kk - 2) * 8);
-                    const uint64_t bd = smem_desc(sbase + C::OFF_ONES + kk * 32, 1024, kSwizzle128B);
-                    mma_f8_ts(tmem + C::COL_R, a, bd, IDESC_RS, kk > 0 ? 1u : 0u);
+                    const uint64_t bd = smem_desc(sbase + C::OFF_ONES + slot * 2048 + kk * 32, 1024, kSwizzle128B);
+                    mma_f8_ts(tmem + C::COL_R, a, bd, IDESC_RS, (slot > 0 || kk > 0) ? 1u : 0u);
+                }
+            };
+            auto issue_mean = [&](int batch) {
+                const uint32_t bmb = sbase + C::OFF_BM + (batch & 1) * C::BMB;
+#pragma unroll
+                for (int i = 0; i < kMeanK / 16; ++i) {
+                    const uint64_t bd = smem_desc_lbo(bmb + i * 256, 128, C::BM_ROW_GROUP, kSwizzleNone);
+                    mma_bf16_ts(tmem + C::COL_O, tmem + C::COL_AM + i * 8, bd, IDESC_MEAN, 1u);
                 }
             };
             bool ok = mbar_wait(bar(C::B_Q), 0, abort_flag, p.dev_status, tmo) &&
@@ -263,16 +309,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; ok && j < J; ++j) {
                 if (j + 1 < J) {
                     const int s1 = (j + 1) % NS;
-                    if (!mbar_wait(bar(C::B_KVF + s1), ((j + 1) / NS) & 1, abort_flag, p.dev_status, tmo)) break;
+                    if (!mbar_wait(bar(C::B_KVF + s1), ((j + 1) / NS) & 1, abort_flag, p.dev_status, tmo)) {
+                        ok = false;
+                        break;
+                    }
                     tc_fence_after();
                     issue_qk(j + 1);
                     mma_commit(bar(C::B_SF + ((j + 1) & 1)));
                 }
-                if (!mbar_wait(bar(C::B_PF + (j & 1)), (j >> 1) & 1, abort_flag, p.dev_status, tmo)) break;
+                if (!mbar_wait(bar(C::B_PF + (j & 1)), (j >> 1) & 1, abort_flag, p.dev_status, tmo)) {
+                    ok = false;
+                    break;
+                }
                 tc_fence_after();
+                if (VSMOOTH && j > 0 && (j % kBatch) == 0) issue_mean(j / kBatch - 1);
                 issue_pv_rs(j);
                 mma_commit(bar(C::B_OD));
                 mma_commit(bar(C::B_KVE + j % NS));
+            }
+            if (VSMOOTH && ok && mbar_wait(bar(C::B_PL), 0, abort_flag, p.dev_status, tmo)) {
+                tc_fence_after();
+                issue_mean((J - 1) / kBatch);
+                mma_commit(bar(C::B_OF));
             }
             // every MMA this thread issued has completed once this phase flips
             mma_commit(bar(C::B_TD));
@@ -289,23 +347,56 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int tail = p.N - (J - 1) * 128;  // valid keys of the last tile, 1..128
         const bool dbg_cta = DBG && bh == p.dbg_bh && qtile == p.dbg_qtile;
         float* xch = reinterpret_cast<float*>(smem + C::OFF_XCH);
+        float* mt = reinterpret_cast<float*>(smem + C::OFF_MT) + wg * kBatch * 128 + row;  // [slot * 128]
         float m = -INFINITY, l = 0.f;
-        float macc[HD];
-#pragma unroll
-        for (int c = 0; c < HD; ++c) macc[c] = 0.f;
-        float sk_next = __ldg(p.sk + (int64_t)bh * p.nblk);
         bool ok = true;
+
+        // Closes a batch of `nslots` tiles: their row sums, rescaled to the running
+        // max m_now, go into l and (warpgroup 0, V-Smooth) into the bf16 A operand
+        // of the mean MMA as hi/lo pairs: k = 3t -> hi, 3t+1 -> lo, 3t+2 -> hi.
+        auto close_batch = [&](float m_now, int nslots) {
+            uint32_t r[16];
+            tmem_ld16(lane_addr + C::COL_R, r);
+            tmem_wait_ld();
+            float rh[kBatch];
+            float lsum = 0.f;
+#pragma unroll
+            for (int t = 0; t < kBatch; ++t) {
+                rh[t] = (t < nslots) ? __uint_as_float(r[t]) * ex2_approx(mt[t * 128] - m_now) : 0.f;
+                lsum += rh[t];
+            }
+            l += lsum;
+            if (VSMOOTH && wg == 0) {
+                uint32_t e[kMeanK];
+#pragma unroll
+                for (int t = 0; t < kBatch; ++t) {
+                    const uint32_t hi = bf16_rn_bits(rh[t]);
+                    const uint32_t lo = bf16_rn_bits(__fsub_rn(rh[t], bf16_bits_to_f32(hi)));
+                    e[3 * t] = hi;
+                    e[3 * t + 1] = lo;
+                    e[3 * t + 2] = hi;
+                }
+                uint32_t a0[16], a1[8];
+#pragma unroll
+                for (int w = 0; w < 16; ++w) a0[w] = e[2 * w] | (e[2 * w + 1] << 16);
+#pragma unroll
+                for (int w = 0; w < 8; ++w) a1[w] = e[32 + 2 * w] | (e[33 + 2 * w] << 16);
+                tmem_st16(lane_addr + C::COL_AM, a0);
+                tmem_st8(lane_addr + C::COL_AM + 16, a1);
+                tmem_wait_st();
+            }
+        };
+
         for (int j = 0; j < J; ++j) {
-            const int sb = j & 1;
+            const int sb = j & 1, slot = j % kBatch;
             const uint32_t colS = sb ? C::COL_S1 : C::COL_S0;
-            const float sk_j = sk_next;
-            if (j + 1 < J) sk_next = __ldg(p.sk + (int64_t)bh * p.nblk + j + 1);
-            if (!mbar_wait(bar(C::B_SF + sb), (j >> 1) & 1, abort_flag, p.dev_status, tmo)) { ok = false; break; }
-            if (VSMOOTH && !mbar_wait(bar(C::B_KVF + j % NS), (j / NS) & 1, abort_flag, p.dev_status, tmo)) {
+            if (!mbar_wait(bar(C::B_SF + sb), (j >> 1) & 1, abort_flag, p.dev_status, tmo) ||
+                !mbar_wait(bar(C::B_KVF + j % NS), (j / NS) & 1, abort_flag, p.dev_status, tmo)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
+            const float sk_j = *reinterpret_cast<const float*>(smem + C::OFF_SK + (j % NS) * 16);
             float a[64];
             {
                 uint32_t r0[32], r1[32];
@@ -329,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int i = 0; i < 64; ++i)
                     if (wg * 64 + i >= tail) a[i] = -INFINITY;
             }
-            // partial row max over this thread's 64 keys
+            // partial row max over this thread's 64 keys, exchanged with the other half
             float mx;
             {
                 float t[22];
@@ -344,7 +435,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             xch[sb * 256 + wg * 128 + row] = mx;
             mbar_arrive(bar(C::B_XCH + sb));
-            if (!mbar_wait(bar(C::B_XCH + sb), (j >> 1) & 1, abort_flag, p.dev_status, tmo)) { ok = false; break; }
+            if (!mbar_wait(bar(C::B_XCH + sb), (j >> 1) & 1, abort_flag, p.dev_status, tmo)) {
+                ok = false;
+                break;
+            }
             const float mx_all = fmaxf(mx, xch[sb * 256 + (1 - wg) * 128 + row]);
             const float sigma = __fmul_rn(__fmul_rn(sq_i, sk_j), p.kscale);
             const float m_new = fmaxf(m, __fmul_rn(sigma, mx_all));
@@ -373,7 +467,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         u2 = min(u2 & 0xFFu, 120u);
                         u3 = min(u3 & 0xFFu, 120u);
                     }
-                    pw[w] = prmt(prmt(u0, u1, 0x0040u), prmt(u2, u3, 0x0040u), 0x5410u);
+                    // low 16 bits of u0 + 256 u1 are c0 | c1 << 8 (the magic's low 16 bits are 0)
+                    pw[w] = prmt(mad_lo(u1, 256u, u0), mad_lo(u3, 256u, u2), 0x5410u);
                 }
             } else {
                 const float off = __fsub_rn(8.f, m_new);
@@ -403,46 +498,37 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tmem_st16(lane_addr + colS + wg * 64, pw);
             tmem_wait_st();
-            if (j > 0) {
-                if (!mbar_wait(bar(C::B_OD), (j - 1) & 1, abort_flag, p.dev_status, tmo)) { ok = false; break; }
+            // O must hold every product up to tile j-1 before it is rescaled, and
+            // the row sums of a finished batch are read after their MMAs complete.
+            const bool resc = (j > 0) && __any_sync(0xffffffffu, alpha != 1.f);
+            const bool bend = (j > 0) && slot == 0;
+            if (resc || bend) {
+                if (!mbar_wait(bar(C::B_OD), (j - 1) & 1, abort_flag, p.dev_status, tmo)) {
+                    ok = false;
+                    break;
+                }
                 tc_fence_after();
-                uint32_t rbits;
-                tmem_ld1(lane_addr + C::COL_R, rbits);
-                tmem_wait_ld();
-                const float r_prev = __uint_as_float(rbits);
-                const bool rescale = __any_sync(0xffffffffu, alpha != 1.f);
-                if (VSMOOTH) {
-                    const float* mu_prev =
-                        reinterpret_cast<const float*>(smem + C::OFF_MU + ((j - 1) % NS) * D * 4) + wg * HD;
-#pragma unroll
-                    for (int c = 0; c < HD; c += 4) {
-                        const float4 mv = *reinterpret_cast<const float4*>(mu_prev + c);
-                        macc[c + 0] = __fmaf_rn(r_prev, mv.x, macc[c + 0]);
-                        macc[c + 1] = __fmaf_rn(r_prev, mv.y, macc[c + 1]);
-                        macc[c + 2] = __fmaf_rn(r_prev, mv.z, macc[c + 2]);
-                        macc[c + 3] = __fmaf_rn(r_prev, mv.w, macc[c + 3]);
-                    }
-                    if (rescale) {
-#pragma unroll
-                        for (int c = 0; c < HD; ++c) macc[c] *= alpha;
-                    }
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bar(C::B_MUE + (j - 1) % NS));
-                }
-                l = alpha * (l + r_prev);
-                if (rescale) {
-#pragma unroll
-                    for (int c0 = 0; c0 < HD; c0 += 32) {
-                        uint32_t o[32];
-                        tmem_ld32(lane_addr + C::COL_O + wg * HD + c0, o);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                        tmem_st32(lane_addr + C::COL_O + wg * HD + c0, o);
-                    }
-                    tmem_wait_st();
-                }
             }
+            if (resc) {
+#pragma unroll
+                for (int c0 = 0; c0 < HD; c0 += 32) {
+                    uint32_t o[32];
+                    tmem_ld32(lane_addr + C::COL_O + wg * HD + c0, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; i += 2) {
+                        const float2 v = __fmul2_rn(make_float2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])),
+                                                    make_float2(alpha, alpha));
+                        o[i] = __float_as_uint(v.x);
+                        o[i + 1] = __float_as_uint(v.y);
+                    }
+                    tmem_st32(lane_addr + C::COL_O + wg * HD + c0, o);
+                }
+                tmem_wait_st();
+            }
+            l *= alpha;
+            if (bend) close_batch(m_new, kBatch);
+            mt[slot * 128] = m_new;
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(C::B_PF + sb));
@@ -450,39 +536,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (ok && mbar_wait(bar(C::B_OD), (J - 1) & 1, abort_flag, p.dev_status, tmo)) {
             tc_fence_after();
-            uint32_t rbits;
-            tmem_ld1(lane_addr + C::COL_R, rbits);
-            tmem_wait_ld();
-            const float r_last = __uint_as_float(rbits);
-            l += r_last;
+            close_batch(m, (J - 1) % kBatch + 1);
+            bool fin = true;
             if (VSMOOTH) {
-                const float* mu_last =
-                    reinterpret_cast<const float*>(smem + C::OFF_MU + ((J - 1) % NS) * D * 4) + wg * HD;
-#pragma unroll
-                for (int c = 0; c < HD; ++c) macc[c] = __fmaf_rn(r_last, mu_last[c], macc[c]);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(C::B_PL));
+                fin = mbar_wait(bar(C::B_OF), 0, abort_flag, p.dev_status, tmo);
+                tc_fence_after();
             }
-            const float inv_l = __frcp_rn(l);
-            const float* svp = p.sv + (int64_t)bh * D + wg * HD;
-            uint16_t* dst = p.O + (int64_t)b * p.o_sb + (int64_t)qrow * p.o_sn + (int64_t)h * p.o_sh + wg * HD;
+            if (fin) {
+                const float inv_l = __frcp_rn(l);
+                const float* svp = p.sv + (int64_t)bh * D + wg * HD;
+                uint16_t* dst =
+                    p.O + (int64_t)b * p.o_sb + (int64_t)qrow * p.o_sn + (int64_t)h * p.o_sh + wg * HD;
 #pragma unroll
-            for (int c0 = 0; c0 < HD; c0 += 32) {
-                uint32_t o[32];
-                tmem_ld32(lane_addr + C::COL_O + wg * HD + c0, o);
-                tmem_wait_ld();
-                uint32_t packed[16];
+                for (int c0 = 0; c0 < HD; c0 += 32) {
+                    uint32_t o[32];
+                    tmem_ld32(lane_addr + C::COL_O + wg * HD + c0, o);
+                    tmem_wait_ld();
+                    uint32_t packed[16];
 #pragma unroll
-                for (int i = 0; i < 32; i += 2) {
-                    const float v0 = __fmaf_rn(__ldg(svp + c0 + i), __uint_as_float(o[i]), macc[c0 + i]) * inv_l;
-                    const float v1 =
-                        __fmaf_rn(__ldg(svp + c0 + i + 1), __uint_as_float(o[i + 1]), macc[c0 + i + 1]) * inv_l;
-                    const __nv_bfloat162 pr = __floats2bfloat162_rn(v0, v1);
-                    packed[i / 2] = *reinterpret_cast<const uint32_t*>(&pr);
-                }
-                if (qrow < p.N) {
-                    uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
+                    for (int i = 0; i < 32; i += 2) {
+                        const float s0 = __ldg(svp + c0 + i), s1 = __ldg(svp + c0 + i + 1);
+                        const float g0 = s0 > 0.f ? s0 : 1.f, g1 = s1 > 0.f ? s1 : 1.f;
+                        const float v0 = g0 * __uint_as_float(o[i]) * inv_l;
+                        const float v1 = g1 * __uint_as_float(o[i + 1]) * inv_l;
+                        const __nv_bfloat162 pr = __floats2bfloat162_rn(v0, v1);
+                        packed[i / 2] = *reinterpret_cast<const uint32_t*>(&pr);
+                    }
+                    if (qrow < p.N) {
+                        uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
 #pragma unroll
-                    for (int v = 0; v < 4; ++v)
-                        d4[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
+                        for (int v = 0; v < 4; ++v)
+                            d4[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
+                    }
                 }
             }
         }

@@ -53,12 +53,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Shared abort state of one CTA: once any thread's wait runs out, every other
-// wait in the CTA returns false at its next poll, so all roles reach teardown.
-struct AbortState {
-    int flag;
-};
-
 // Bounded wait on an mbarrier phase.  Returns false (and raises the CTA's
 // abort flag and writes VC_ERR_TIMEOUT to *dev_status) if the phase has not
 // completed within timeout_ns, or if another thread of the CTA gave up.
@@ -69,9 +63,9 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     uint32_t spins = 0;
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (*abort_flag) return false;
-        if ((++spins & 63u) == 0) {
-            if (globaltimer_ns() - t0 > timeout_ns) {
+        if ((++spins & 15u) == 0) {
+            if (*abort_flag) return false;
+            if ((spins & 255u) == 0 && globaltimer_ns() - t0 > timeout_ns) {
                 *abort_flag = 1;
                 if (dev_status) atomicMax(reinterpret_cast<int*>(dev_status), (int)VC_ERR_TIMEOUT);
                 return false;
@@ -160,6 +154,20 @@ __device__ __forceinline__ void tmem_ld1(uint32_t taddr, uint32_t& r) {
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr));
 }
 
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
+                 "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
+}
+
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
@@ -200,6 +208,37 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t sbo_bytes
     return d;
 }
 
+enum : uint32_t { kSwizzleNone = 0 };
+
+// Same descriptor with an explicit leading-dimension byte offset (used by the
+// non-swizzled K-major layout: core matrices of 8 rows x 16 bytes, LBO = step
+// between core matrices along K, SBO = step between groups of 8 rows).
+__device__ __forceinline__ uint64_t smem_desc_lbo(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes,
+                                                  uint32_t layout) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1u << 46;
+    d |= (uint64_t)(layout & 7u) << 61;
+    return d;
+}
+
+// Instruction descriptor, kind::f16 with A = B = BF16 (format 1 at bits 7-9 and 10-12), D = F32.
+__host__ __device__ constexpr uint32_t idesc_bf16(uint32_t M, uint32_t N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+// D[tmem] (+)= A[tmem] * B[smem desc]^T, kind::f16 (BF16 x BF16 -> F32).
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Instruction descriptor, kind::f8f6f4, A = B = E4M3, D = F32, both K-major.
 // Bits: D format (4-5) = 1 (F32); A format (7-9) = 0 (E4M3); B format (10-12) = 0;
 // no negation, no transpose; N >> 3 at bits 17-22; M >> 4 at bits 24-28.
@@ -224,6 +263,13 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     uint32_t r;
     asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+    return r;
+}
+
+// a * b + c on 32-bit integers (kept as one multiply-add so it issues on the FMA pipe).
+__device__ __forceinline__ uint32_t mad_lo(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t r;
+    asm("mad.lo.u32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
     return r;
 }
 

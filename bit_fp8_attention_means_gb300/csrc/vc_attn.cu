@@ -30,7 +30,8 @@
 // parts and the MMA thread adds sum_t r_t mu_t^T to O with one bf16 MMA of
 // depth 48 (terms r_hi mu_hi + r_lo mu_hi + r_hi mu_lo per tile).  The means
 // enter in units of the channel's residual scale g_c (g_c = s_v[c], or 1 for a
-// channel whose residual is identically 0), so O = g (.) A / l at the end.
+// channel whose residual is identically 0; mu' = mu * fp32(1/g_c)), so
+// O = g (.) A / l at the end.
 // The normaliser l is kept in registers, updated from the same row sums.
 //
 // ExpCast inner loop, per score: ts = sat(acc * sigma/16 + C/128) (one FFMA
@@ -157,7 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 16);
 
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0), lane = threadIdx.x & 31;
     const int qtile = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int bh = b * p.H + h;
     const int J = p.nblk;
@@ -202,17 +203,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
+    const uint32_t tmem = __shfl_sync(0xffffffffu, *tmem_slot, 0);
 
     if (warp == kProducerWarp) {
         // ------------------------------------------------------------ producer
         const int32_t row0 = (int32_t)((int64_t)bh * p.Npad);
         constexpr int PER = D / 32;  // channels per lane for the mean operand
-        float g_ch[PER];
+        float ginv[PER];             // 1 / g_c, g_c = s_v[c] (1 for an all-zero residual channel)
 #pragma unroll
         for (int e = 0; e < PER; ++e) {
             const float sv = __ldg(p.sv + (int64_t)bh * D + lane * PER + e);
-            g_ch[e] = sv > 0.f ? sv : 1.f;
+            ginv[e] = __frcp_rn(sv > 0.f ? sv : 1.f);
         }
         if (lane == 0) {
             prefetch_tensormap(&tmQ);
@@ -225,22 +226,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         int issued = 0;
         for (int j = 0; j < J; ++j) {
             const int s = j % NS, n = j / NS;
-            if (j >= NS && !mbar_wait(bar(C::B_KVE + s), (n - 1) & 1, abort_flag, p.dev_status, tmo)) break;
+            // global loads for this tile go out before the wait for a free stage,
+            // so their latency overlaps it
+            const float sk_j = (lane == 0) ? __ldg(p.sk + (int64_t)bh * p.nblk + j) : 0.f;
+            uint32_t mu_w[PER / 2];
+            if (VSMOOTH) {
+                const uint32_t* src =
+                    reinterpret_cast<const uint32_t*>(p.mu + ((int64_t)bh * p.nblk + j) * D + lane * PER);
+#pragma unroll
+                for (int e = 0; e < PER / 2; ++e) mu_w[e] = __ldg(src + e);
+            }
+            if (j >= NS && !mbar_wait_warp(bar(C::B_KVE + s), (n - 1) & 1, abort_flag, p.dev_status, tmo)) break;
             if (lane == 0) {
                 mbar_expect_tx(bar(C::B_KVF + s), C::KB + C::VB);
                 tma_load_2d(sbase + C::OFF_K + s * C::KB, &tmK, 0, row0 + j * 128, bar(C::B_KVF + s));
                 tma_load_2d(sbase + C::OFF_V + s * C::VB, &tmV, j * 128, bh * D, bar(C::B_KVF + s));
-                *reinterpret_cast<float*>(smem + C::OFF_SK + s * 16) = __ldg(p.sk + (int64_t)bh * p.nblk + j);
+                *reinterpret_cast<float*>(smem + C::OFF_SK + s * 16) = sk_j;
             }
             if (VSMOOTH) {
                 // mean operand rows: k = 3t, 3t+1, 3t+2 hold (mu'_hi, mu'_hi, mu'_lo), mu' = mu / g
                 uint8_t* bmb = smem + C::OFF_BM + ((j / kBatch) & 1) * C::BMB;
                 const int k0 = 3 * (j % kBatch);
-                const uint16_t* src = p.mu + ((int64_t)bh * p.nblk + j) * D + lane * PER;
 #pragma unroll
                 for (int e = 0; e < PER; ++e) {
                     const int n_ch = lane * PER + e;
-                    const float mp = __fdiv_rn(bf16_bits_to_f32(__ldg(src + e)), g_ch[e]);
+                    const uint32_t bits = (e & 1) ? (mu_w[e / 2] >> 16) : (mu_w[e / 2] & 0xFFFFu);
+                    const float mp = __fmul_rn(bf16_bits_to_f32(bits), ginv[e]);
                     const uint16_t hi = bf16_rn_bits(mp);
                     const uint16_t lo = bf16_rn_bits(__fsub_rn(mp, bf16_bits_to_f32(hi)));
                     *reinterpret_cast<uint16_t*>(bmb + bm_offset(n_ch, k0)) = hi;
@@ -259,7 +270,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         drain_wait(bar(C::B_Q), 0, tmo);
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        // The whole warp runs this loop (uniform control flow); each tensor-core
+        // instruction is issued by one elected lane.
+        {
             constexpr uint32_t IDESC_QK = idesc_f8_e4m3(128, 128);
             constexpr uint32_t IDESC_PV = idesc_f8_e4m3(128, D);
             constexpr uint32_t IDESC_RS = idesc_f8_e4m3(128, 16);
@@ -271,7 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kk = 0; kk < D / 32; ++kk) {
                     const uint64_t ad = smem_desc(sbase + C::OFF_Q + kk * 32, C::QK_SBO, C::QK_SWZ);
                     const uint64_t bd = smem_desc(sbase + C::OFF_K + s * C::KB + kk * 32, C::QK_SBO, C::QK_SWZ);
-                    mma_f8_ss(d, ad, bd, IDESC_QK, kk > 0 ? 1u : 0u);
+                    mma_f8_ss_w(d, ad, bd, IDESC_QK, kk > 0 ? 1u : 0u);
                 }
             };
             auto issue_pv_rs = [&](int j) {
@@ -282,13 +295,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kk = 0; kk < 4; ++kk) {
                     const uint32_t a = pbase + (kk < 2 ? kk * 8 : 64 + (kk - 2) * 8);
                     const uint64_t bd = smem_desc(sbase + C::OFF_V + s * C::VB + kk * 32, 1024, kSwizzle128B);
-                    mma_f8_ts(tmem + C::COL_O, a, bd, IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+                    mma_f8_ts_w(tmem + C::COL_O, a, bd, IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
                 }
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
                     const uint32_t a = pbase + (kk < 2 ? kk * 8 : 64 + (kk - 2) * 8);
                     const uint64_t bd = smem_desc(sbase + C::OFF_ONES + slot * 2048 + kk * 32, 1024, kSwizzle128B);
-                    mma_f8_ts(tmem + C::COL_R, a, bd, IDESC_RS, (slot > 0 || kk > 0) ? 1u : 0u);
+                    mma_f8_ts_w(tmem + C::COL_R, a, bd, IDESC_RS, (slot > 0 || kk > 0) ? 1u : 0u);
                 }
             };
             auto issue_mean = [&](int batch) {
@@ -296,44 +309,44 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int i = 0; i < kMeanK / 16; ++i) {
                     const uint64_t bd = smem_desc_lbo(bmb + i * 256, 128, C::BM_ROW_GROUP, kSwizzleNone);
-                    mma_bf16_ts(tmem + C::COL_O, tmem + C::COL_AM + i * 8, bd, IDESC_MEAN, 1u);
+                    mma_bf16_ts_w(tmem + C::COL_O, tmem + C::COL_AM + i * 8, bd, IDESC_MEAN, 1u);
                 }
             };
-            bool ok = mbar_wait(bar(C::B_Q), 0, abort_flag, p.dev_status, tmo) &&
-                      mbar_wait(bar(C::B_KVF), 0, abort_flag, p.dev_status, tmo);
+            bool ok = mbar_wait_warp(bar(C::B_Q), 0, abort_flag, p.dev_status, tmo) &&
+                      mbar_wait_warp(bar(C::B_KVF), 0, abort_flag, p.dev_status, tmo);
             if (ok) {
                 tc_fence_after();
                 issue_qk(0);
-                mma_commit(bar(C::B_SF + 0));
+                mma_commit_w(bar(C::B_SF + 0));
             }
             for (int j = 0; ok && j < J; ++j) {
                 if (j + 1 < J) {
                     const int s1 = (j + 1) % NS;
-                    if (!mbar_wait(bar(C::B_KVF + s1), ((j + 1) / NS) & 1, abort_flag, p.dev_status, tmo)) {
+                    if (!mbar_wait_warp(bar(C::B_KVF + s1), ((j + 1) / NS) & 1, abort_flag, p.dev_status, tmo)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     issue_qk(j + 1);
-                    mma_commit(bar(C::B_SF + ((j + 1) & 1)));
+                    mma_commit_w(bar(C::B_SF + ((j + 1) & 1)));
                 }
-                if (!mbar_wait(bar(C::B_PF + (j & 1)), (j >> 1) & 1, abort_flag, p.dev_status, tmo)) {
+                if (!mbar_wait_warp(bar(C::B_PF + (j & 1)), (j >> 1) & 1, abort_flag, p.dev_status, tmo)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 if (VSMOOTH && j > 0 && (j % kBatch) == 0) issue_mean(j / kBatch - 1);
                 issue_pv_rs(j);
-                mma_commit(bar(C::B_OD));
-                mma_commit(bar(C::B_KVE + j % NS));
+                mma_commit_w(bar(C::B_OD));
+                mma_commit_w(bar(C::B_KVE + j % NS));
             }
-            if (VSMOOTH && ok && mbar_wait(bar(C::B_PL), 0, abort_flag, p.dev_status, tmo)) {
+            if (VSMOOTH && ok && mbar_wait_warp(bar(C::B_PL), 0, abort_flag, p.dev_status, tmo)) {
                 tc_fence_after();
                 issue_mean((J - 1) / kBatch);
-                mma_commit(bar(C::B_OF));
+                mma_commit_w(bar(C::B_OF));
             }
             // every MMA this thread issued has completed once this phase flips
-            mma_commit(bar(C::B_TD));
+            mma_commit_w(bar(C::B_TD));
             drain_wait(bar(C::B_TD), 0, tmo);
         }
         __syncwarp();
@@ -390,8 +403,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < J; ++j) {
             const int sb = j & 1, slot = j % kBatch;
             const uint32_t colS = sb ? C::COL_S1 : C::COL_S0;
-            if (!mbar_wait(bar(C::B_SF + sb), (j >> 1) & 1, abort_flag, p.dev_status, tmo) ||
-                !mbar_wait(bar(C::B_KVF + j % NS), (j / NS) & 1, abort_flag, p.dev_status, tmo)) {
+            if (!mbar_wait_warp(bar(C::B_SF + sb), (j >> 1) & 1, abort_flag, p.dev_status, tmo) ||
+                !mbar_wait_warp(bar(C::B_KVF + j % NS), (j / NS) & 1, abort_flag, p.dev_status, tmo)) {
                 ok = false;
                 break;
             }
@@ -435,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             xch[sb * 256 + wg * 128 + row] = mx;
             mbar_arrive(bar(C::B_XCH + sb));
-            if (!mbar_wait(bar(C::B_XCH + sb), (j >> 1) & 1, abort_flag, p.dev_status, tmo)) {
+            if (!mbar_wait_warp(bar(C::B_XCH + sb), (j >> 1) & 1, abort_flag, p.dev_status, tmo)) {
                 ok = false;
                 break;
             }
@@ -503,7 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool resc = (j > 0) && __any_sync(0xffffffffu, alpha != 1.f);
             const bool bend = (j > 0) && slot == 0;
             if (resc || bend) {
-                if (!mbar_wait(bar(C::B_OD), (j - 1) & 1, abort_flag, p.dev_status, tmo)) {
+                if (!mbar_wait_warp(bar(C::B_OD), (j - 1) & 1, abort_flag, p.dev_status, tmo)) {
                     ok = false;
                     break;
                 }
@@ -534,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive(bar(C::B_PF + sb));
             m = m_new;
         }
-        if (ok && mbar_wait(bar(C::B_OD), (J - 1) & 1, abort_flag, p.dev_status, tmo)) {
+        if (ok && mbar_wait_warp(bar(C::B_OD), (J - 1) & 1, abort_flag, p.dev_status, tmo)) {
             tc_fence_after();
             close_batch(m, (J - 1) % kBatch + 1);
             bool fin = true;
@@ -542,7 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(C::B_PL));
-                fin = mbar_wait(bar(C::B_OF), 0, abort_flag, p.dev_status, tmo);
+                fin = mbar_wait_warp(bar(C::B_OF), 0, abort_flag, p.dev_status, tmo);
                 tc_fence_after();
             }
             if (fin) {

@@ -41,6 +41,7 @@
 // The upper clip at 120 is implied while |m'| < 2^19 (t <= 119.65 + 2^-1);
 // rows beyond take a path with an explicit min.
 #include <cstdio>
+#include <type_traits>
 
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
@@ -140,6 +141,28 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64
 // core matrices of 8 rows x 8 bf16 (16 bytes), 6 along K per group of 8 rows.
 __device__ __forceinline__ uint32_t bm_offset(int n, int k) {
     return (uint32_t)((n >> 3) * (6 * 128) + (k >> 3) * 128 + (n & 7) * 16 + (k & 7) * 2);
+}
+
+// Four ExpCast bytes, packed little-endian.  ts = sat(acc k1 + k2) is t/128
+// clipped to [0, 1]; ts*128 + 1.5*2^23 puts rint(t) in the low byte.
+template <bool CLIP>
+__device__ __forceinline__ uint32_t expcast4(const float* a, float k1, float k2) {
+    const float t0 = fma_sat(a[0], k1, k2);
+    const float t1 = fma_sat(a[1], k1, k2);
+    const float t2 = fma_sat(a[2], k1, k2);
+    const float t3 = fma_sat(a[3], k1, k2);
+    const float2 b01 = __ffma2_rn(make_float2(t0, t1), make_float2(128.f, 128.f), make_float2(kMagic, kMagic));
+    const float2 b23 = __ffma2_rn(make_float2(t2, t3), make_float2(128.f, 128.f), make_float2(kMagic, kMagic));
+    uint32_t u0 = __float_as_uint(b01.x), u1 = __float_as_uint(b01.y);
+    uint32_t u2 = __float_as_uint(b23.x), u3 = __float_as_uint(b23.y);
+    if (CLIP) {
+        u0 = min(u0 & 0xFFu, 120u);
+        u1 = min(u1 & 0xFFu, 120u);
+        u2 = min(u2 & 0xFFu, 120u);
+        u3 = min(u3 & 0xFFu, 120u);
+    }
+    // low 16 bits of u0 + 256 u1 are c0 | c1 << 8 (the magic's low 16 bits are 0)
+    return prmt(mad_lo(u1, 256u, u0), mad_lo(u3, 256u, u2), 0x5410u);
 }
 
 __device__ __forceinline__ uint16_t bf16_rn_bits(float x) { return __bfloat16_as_ushort(__float2bfloat16_rn(x)); }
@@ -400,13 +423,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         };
 
-        for (int j = 0; j < J; ++j) {
+        // One key tile.  MASKED is set only for the last tile, so the hot loop
+        // carries no masking code.  Returns false when a wait gave up.
+        auto step = [&](int j, auto masked_tag) -> bool {
+            constexpr bool MASKED = decltype(masked_tag)::value;
             const int sb = j & 1, slot = j % kBatch;
             const uint32_t colS = sb ? C::COL_S1 : C::COL_S0;
             if (!mbar_wait_warp(bar(C::B_SF + sb), (j >> 1) & 1, abort_flag, p.dev_status, tmo) ||
                 !mbar_wait_warp(bar(C::B_KVF + j % NS), (j / NS) & 1, abort_flag, p.dev_status, tmo)) {
-                ok = false;
-                break;
+                return false;
             }
             tc_fence_after();
             const float sk_j = *reinterpret_cast<const float*>(smem + C::OFF_SK + (j % NS) * 16);
@@ -427,7 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int i = 0; i < 64; ++i) dst[i] = a[i];
             }
-            const bool masked = (j == J - 1) && (tail < 128);
+            const bool masked = MASKED && (tail < 128);
             if (masked) {
 #pragma unroll
                 for (int i = 0; i < 64; ++i)
@@ -449,8 +474,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             xch[sb * 256 + wg * 128 + row] = mx;
             mbar_arrive(bar(C::B_XCH + sb));
             if (!mbar_wait_warp(bar(C::B_XCH + sb), (j >> 1) & 1, abort_flag, p.dev_status, tmo)) {
-                ok = false;
-                break;
+                return false;
             }
             const float mx_all = fmaxf(mx, xch[sb * 256 + (1 - wg) * 128 + row]);
             const float sigma = __fmul_rn(__fmul_rn(sq_i, sk_j), p.kscale);
@@ -461,27 +485,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float Cc = __fmaf_rn(-8.f, m_new, 119.65f);
                 const float k1 = sigma * 0.0625f;
                 const float k2 = Cc * 0.0078125f;
-                const bool fast = fabsf(m_new) < 524288.f;
+                // |m'| < 2^19 in every row of the warp: the clip at 120 is implied
+                if (__all_sync(0xffffffffu, fabsf(m_new) < 524288.f)) {
 #pragma unroll
-                for (int w = 0; w < 16; ++w) {
-                    const float t0 = fma_sat(a[4 * w + 0], k1, k2);
-                    const float t1 = fma_sat(a[4 * w + 1], k1, k2);
-                    const float t2 = fma_sat(a[4 * w + 2], k1, k2);
-                    const float t3 = fma_sat(a[4 * w + 3], k1, k2);
-                    const float2 b01 = __ffma2_rn(make_float2(t0, t1), make_float2(128.f, 128.f),
-                                                  make_float2(kMagic, kMagic));
-                    const float2 b23 = __ffma2_rn(make_float2(t2, t3), make_float2(128.f, 128.f),
-                                                  make_float2(kMagic, kMagic));
-                    uint32_t u0 = __float_as_uint(b01.x), u1 = __float_as_uint(b01.y);
-                    uint32_t u2 = __float_as_uint(b23.x), u3 = __float_as_uint(b23.y);
-                    if (!fast) {
-                        u0 = min(u0 & 0xFFu, 120u);
-                        u1 = min(u1 & 0xFFu, 120u);
-                        u2 = min(u2 & 0xFFu, 120u);
-                        u3 = min(u3 & 0xFFu, 120u);
-                    }
-                    // low 16 bits of u0 + 256 u1 are c0 | c1 << 8 (the magic's low 16 bits are 0)
-                    pw[w] = prmt(mad_lo(u1, 256u, u0), mad_lo(u3, 256u, u2), 0x5410u);
+                    for (int w = 0; w < 16; ++w) pw[w] = expcast4<false>(a + 4 * w, k1, k2);
+                } else {
+#pragma unroll
+                    for (int w = 0; w < 16; ++w) pw[w] = expcast4<true>(a + 4 * w, k1, k2);
                 }
             } else {
                 const float off = __fsub_rn(8.f, m_new);
@@ -517,8 +527,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool bend = (j > 0) && slot == 0;
             if (resc || bend) {
                 if (!mbar_wait_warp(bar(C::B_OD), (j - 1) & 1, abort_flag, p.dev_status, tmo)) {
-                    ok = false;
-                    break;
+                    return false;
                 }
                 tc_fence_after();
             }
@@ -546,7 +555,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(C::B_PF + sb));
             m = m_new;
-        }
+            return true;
+        };
+        for (int j = 0; j < J - 1; ++j)
+            if (!step(j, std::false_type{})) {
+                ok = false;
+                break;
+            }
+        if (ok && !step(J - 1, std::true_type{})) ok = false;
         if (ok && mbar_wait_warp(bar(C::B_OD), (J - 1) & 1, abort_flag, p.dev_status, tmo)) {
             tc_fence_after();
             close_batch(m, (J - 1) % kBatch + 1);

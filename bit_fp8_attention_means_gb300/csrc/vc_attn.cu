@@ -12,19 +12,24 @@
 //              key columns [64 wg, 64 wg + 64) of each 128-key tile and output
 //              channels [wg d/2, (wg+1) d/2).  The halves of a row exchange
 //              partial maxima through shared memory.
-//   warp 8     producer: TMA loads of Q (once) and of the K and V^T tiles
-//              (ring of NS stages); per tile it also writes the key scale and
-//              the block mean, split into bf16 hi/lo parts, into shared memory.
-//   warp 9     MMA issuer (one thread) and TMEM owner.
+//   warp 8     producer: TMA loads of the K and V^T tiles (ring of NS
+//              stages); per tile it also writes the key scale, the
+//              row-sum operand and the block mean (bf16 hi/lo parts) into
+//              shared memory.
+//   warp 9     MMA issuer (one elected lane) and TMEM owner.
 // Tensor memory (512 columns):
 //   S0, S1  [0,256)        fp32 scores of key tile j (double-buffered), QK^T.
 //   P       inside S       probability bytes of tile j overwrite the first 16
 //                          columns of each half of the score buffer.
 //   O       [256, 256+d)   fp32 accumulator in residual-code units.
-//   R       16 columns     row sums r_ij of the last 16 tiles: tile j adds
-//                          P_j * e_(j mod 16) into column j mod 16 (one small
-//                          MMA against a ones operand with a single 1-row).
+//   R       16 columns     row sums r_ij of the last 16 tiles, directly after O.
 //   AM      24 columns     bf16 A operand of the batched mean restore.
+//   Q       d/4 columns    the CTA's Q codes (A operand of every QK MMA),
+//                          written once by the softmax warps.
+// Row sums: each V^T stage carries 16 operand rows after its d channel rows;
+// row d + (j mod 16) holds E4M3 1.0 and the others 0, so the PV MMA of width
+// d + 16 adds P_j V_j into O and r_j into column j mod 16 of R.  The first
+// tile of a batch restarts R with a separate width-16 MMA.
 // Mean restore, batched: every 16 tiles the softmax warps read the 16 row
 // sums, rescale each to the current running max, split them into bf16 hi/lo
 // parts and the MMA thread adds sum_t r_t mu_t^T to O with one bf16 MMA of
@@ -62,19 +67,16 @@ constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23: adding it rounds to an int
 
 template <int D>
 struct Cfg {
-    static constexpr int NS = (D == 128) ? 4 : 6;
-    static constexpr int QB = 128 * D;
+    static constexpr int NS = (D == 128) ? 5 : 6;
     static constexpr int KB = 128 * D;
-    static constexpr int VB = D * 128;
+    static constexpr int VB = (D + 16) * 128;           // d channel rows + 16 row-sum operand rows
     static constexpr uint32_t QK_SWZ = (D == 128) ? kSwizzle128B : kSwizzle64B;
     static constexpr uint32_t QK_SBO = 8 * D;  // bytes per group of 8 rows
     static constexpr int BM_ROW_GROUP = 6 * 128;        // 8 rows x 48 bf16, stored as 6 core matrices
     static constexpr int BMB = (D / 8) * BM_ROW_GROUP;  // one mean-operand buffer
-    static constexpr int OFF_Q = 0;
-    static constexpr int OFF_K = OFF_Q + QB;
+    static constexpr int OFF_K = 0;
     static constexpr int OFF_V = OFF_K + NS * KB;
-    static constexpr int OFF_ONES = OFF_V + NS * VB;     // kBatch ones operands of 16 x 128 bytes
-    static constexpr int OFF_BM = OFF_ONES + kBatch * 2048;
+    static constexpr int OFF_BM = OFF_V + NS * VB;
     static constexpr int OFF_SK = OFF_BM + 2 * BMB;
     static constexpr int OFF_MT = OFF_SK + NS * 16;      // running max per (wg, slot, row)
     static constexpr int OFF_XCH = OFF_MT + 2 * kBatch * 128 * 4;
@@ -85,6 +87,7 @@ struct Cfg {
     // at least 116 KB so that exactly one CTA (and one 512-column TMEM owner) sits on an SM
     static constexpr int SMEM = ((USED > 118784) ? USED : 118784) + 1024;
     static_assert(SMEM <= 232448, "shared memory budget");
+    static_assert(VB % 1024 == 0 && KB % 1024 == 0 && OFF_V % 1024 == 0, "stages keep the swizzle alignment");
     // barrier indices
     static constexpr int B_Q = 0;
     static constexpr int B_KVF = 1;
@@ -100,10 +103,12 @@ struct Cfg {
     static_assert(NBAR_USED <= NBAR, "barrier area");
     // TMEM columns
     static constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O = 256, COL_R = 256 + D, COL_AM = 256 + D + 16;
-    static_assert(COL_AM + kMeanK / 2 <= kTmemCols, "tmem budget");
+    static constexpr uint32_t COL_Q = COL_AM + kMeanK / 2;  // Q codes, 4 per column, D / 4 columns
+    static_assert(COL_Q + D / 4 <= kTmemCols, "tmem budget");
 };
 
 struct AttnParams {
+    const uint8_t* Q8;
     const float* sq;
     const float* sk;
     const float* sv;
@@ -169,8 +174,8 @@ __device__ __forceinline__ uint16_t bf16_rn_bits(float x) { return __bfloat16_as
 
 template <int D, bool EXPCAST, bool VSMOOTH, bool DBG>
 __global__ void __launch_bounds__(kThreads, 1)
-    attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                    const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                    const AttnParams p) {
     using C = Cfg<D>;
     constexpr int NS = C::NS;
     constexpr int HD = D / 2;  // output channels per softmax thread
@@ -188,7 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t tmo = p.timeout_ns;
 
     if (threadIdx.x == 0) {
-        mbar_init(bar(C::B_Q), 1);
+        mbar_init(bar(C::B_Q), 8);  // the eight softmax warps have written Q into TMEM
         for (int s = 0; s < NS; ++s) {
             mbar_init(bar(C::B_KVF + s), 1);
             mbar_init(bar(C::B_KVE + s), 1);
@@ -210,15 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_relinquish();
     }
     {
-        // Ones operands for the row-sum MMA: operand s has row s = E4M3 1.0 (0x38),
-        // all other rows 0, so P_j * operand (j mod 16) adds r_j to column j mod 16.
-        // A 128-byte row is the same under the 128-byte swizzle, so no swizzle
-        // bookkeeping is needed.  The mean operand buffers start zeroed.
-        uint64_t* ones = reinterpret_cast<uint64_t*>(smem + C::OFF_ONES);
-        for (int i = threadIdx.x; i < kBatch * 2048 / 8; i += kThreads) {
-            const int tile = i / 256, row = (i % 256) / 16;
-            ones[i] = (row == tile) ? 0x3838383838383838ull : 0ull;
-        }
+        // The mean operand buffers start zeroed.
         uint4* bm = reinterpret_cast<uint4*>(smem + C::OFF_BM);
         for (int i = threadIdx.x; i < 2 * C::BMB / 16; i += kThreads) bm[i] = make_uint4(0, 0, 0, 0);
         fence_proxy_async_smem();
@@ -239,12 +236,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             ginv[e] = __frcp_rn(sv > 0.f ? sv : 1.f);
         }
         if (lane == 0) {
-            prefetch_tensormap(&tmQ);
             prefetch_tensormap(&tmK);
             prefetch_tensormap(&tmV);
-            mbar_expect_tx(bar(C::B_Q), C::QB);
-            tma_load_2d(sbase + C::OFF_Q, &tmQ, 0, row0 + qtile * 128, bar(C::B_Q));
-            mbar_arrive(bar(C::B_Q));
         }
         int issued = 0;
         for (int j = 0; j < J; ++j) {
@@ -261,10 +254,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (j >= NS && !mbar_wait_warp(bar(C::B_KVE + s), (n - 1) & 1, abort_flag, p.dev_status, tmo)) break;
             if (lane == 0) {
-                mbar_expect_tx(bar(C::B_KVF + s), C::KB + C::VB);
+                mbar_expect_tx(bar(C::B_KVF + s), C::KB + D * 128);
                 tma_load_2d(sbase + C::OFF_K + s * C::KB, &tmK, 0, row0 + j * 128, bar(C::B_KVF + s));
                 tma_load_2d(sbase + C::OFF_V + s * C::VB, &tmV, j * 128, bh * D, bar(C::B_KVF + s));
                 *reinterpret_cast<float*>(smem + C::OFF_SK + s * 16) = sk_j;
+            }
+            {
+                // row-sum operand rows D..D+15 of the stage: row D + (j mod 16) is
+                // E4M3 1.0 (0x38), the others 0, so the PV MMA adds r_j to column
+                // j mod 16 of R.  A uniform 128-byte row is the same under the
+                // 128-byte swizzle.
+                uint4* ones = reinterpret_cast<uint4*>(smem + C::OFF_V + s * C::VB + D * 128);
+                const int slot = j % kBatch;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int idx = lane * 4 + i;  // 16-byte chunk, 8 per row
+                    const uint32_t v = ((idx >> 3) == slot) ? 0x38383838u : 0u;
+                    ones[idx] = make_uint4(v, v, v, v);
+                }
             }
             if (VSMOOTH) {
                 // mean operand rows: k = 3t, 3t+1, 3t+2 hold (mu'_hi, mu'_hi, mu'_lo), mu' = mu / g
@@ -281,8 +288,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     *reinterpret_cast<uint16_t*>(bmb + bm_offset(n_ch, k0 + 1)) = hi;
                     *reinterpret_cast<uint16_t*>(bmb + bm_offset(n_ch, k0 + 2)) = lo;
                 }
-                fence_proxy_async_smem();
             }
+            fence_proxy_async_smem();  // the generic-proxy writes above are read by the MMAs
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(C::B_KVF + s));
             issued = j + 1;
@@ -290,7 +297,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         // let this CTA's own copies in flight land before the CTA can exit
         for (int j = (issued > NS ? issued - NS : 0); j < issued; ++j)
             drain_wait(bar(C::B_KVF + j % NS), (j / NS) & 1, tmo);
-        drain_wait(bar(C::B_Q), 0, tmo);
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
         // The whole warp runs this loop (uniform control flow); each tensor-core
@@ -298,6 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         {
             constexpr uint32_t IDESC_QK = idesc_f8_e4m3(128, 128);
             constexpr uint32_t IDESC_PV = idesc_f8_e4m3(128, D);
+            constexpr uint32_t IDESC_PVR = idesc_f8_e4m3(128, D + 16);  // O and R together
             constexpr uint32_t IDESC_RS = idesc_f8_e4m3(128, 16);
             constexpr uint32_t IDESC_MEAN = idesc_bf16(128, D);
             auto issue_qk = [&](int j) {
@@ -305,26 +312,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t d = tmem + ((j & 1) ? C::COL_S1 : C::COL_S0);
 #pragma unroll
                 for (int kk = 0; kk < D / 32; ++kk) {
-                    const uint64_t ad = smem_desc(sbase + C::OFF_Q + kk * 32, C::QK_SBO, C::QK_SWZ);
                     const uint64_t bd = smem_desc(sbase + C::OFF_K + s * C::KB + kk * 32, C::QK_SBO, C::QK_SWZ);
-                    mma_f8_ss_w(d, ad, bd, IDESC_QK, kk > 0 ? 1u : 0u);
+                    mma_f8_ts_w(d, tmem + C::COL_Q + kk * 8, bd, IDESC_QK, kk > 0 ? 1u : 0u);
                 }
             };
+            // P_j V_j into O and the row sums into R: one MMA of width d + 16 per
+            // K-step reads the stage's channel rows and its row-sum operand rows.
+            // The first tile of a batch restarts R with separate width-d and
+            // width-16 MMAs.
             auto issue_pv_rs = [&](int j) {
                 const int s = j % NS;
                 const uint32_t pbase = tmem + ((j & 1) ? C::COL_S1 : C::COL_S0);
-                const int slot = j % kBatch;
+                const uint32_t vbase = sbase + C::OFF_V + s * C::VB;
+                if (j % kBatch != 0) {
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const uint32_t a = pbase + (kk < 2 ? kk * 8 : 64 + (kk - 2) * 8);
-                    const uint64_t bd = smem_desc(sbase + C::OFF_V + s * C::VB + kk * 32, 1024, kSwizzle128B);
-                    mma_f8_ts_w(tmem + C::COL_O, a, bd, IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
-                }
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint32_t a = pbase + (kk < 2 ? kk * 8 : 64 + (kk - 2) * 8);
+                        const uint64_t bd = smem_desc(vbase + kk * 32, 1024, kSwizzle128B);
+                        mma_f8_ts_w(tmem + C::COL_O, a, bd, IDESC_PVR, 1u);
+                    }
+                } else {
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const uint32_t a = pbase + (kk < 2 ? kk * 8 : 64 + (kk - 2) * 8);
-                    const uint64_t bd = smem_desc(sbase + C::OFF_ONES + slot * 2048 + kk * 32, 1024, kSwizzle128B);
-                    mma_f8_ts_w(tmem + C::COL_R, a, bd, IDESC_RS, (slot > 0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint32_t a = pbase + (kk < 2 ? kk * 8 : 64 + (kk - 2) * 8);
+                        const uint64_t bd = smem_desc(vbase + kk * 32, 1024, kSwizzle128B);
+                        mma_f8_ts_w(tmem + C::COL_O, a, bd, IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+                    }
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint32_t a = pbase + (kk < 2 ? kk * 8 : 64 + (kk - 2) * 8);
+                        const uint64_t bd = smem_desc(vbase + D * 128 + kk * 32, 1024, kSwizzle128B);
+                        mma_f8_ts_w(tmem + C::COL_R, a, bd, IDESC_RS, kk > 0 ? 1u : 0u);
+                    }
                 }
             };
             auto issue_mean = [&](int batch) {
@@ -386,6 +405,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         float* mt = reinterpret_cast<float*>(smem + C::OFF_MT) + wg * kBatch * 128 + row;  // [slot * 128]
         float m = -INFINITY, l = 0.f;
         bool ok = true;
+        {
+            // Q codes of this row into TMEM (column c holds bytes 4c..4c+3), read
+            // by every QK MMA as its A operand; each warpgroup writes half the row.
+            const uint4* src = reinterpret_cast<const uint4*>(
+                p.Q8 + ((int64_t)bh * p.Npad + (int64_t)qtile * 128 + row) * D + wg * (D / 2));
+            uint32_t w[D / 8];
+#pragma unroll
+            for (int i = 0; i < D / 32; ++i) {
+                const uint4 v = __ldg(src + i);
+                w[4 * i] = v.x;
+                w[4 * i + 1] = v.y;
+                w[4 * i + 2] = v.z;
+                w[4 * i + 3] = v.w;
+            }
+            if constexpr (D == 128) tmem_st16(lane_addr + C::COL_Q + wg * (D / 8), w);
+            else tmem_st8(lane_addr + C::COL_Q + wg * (D / 8), w);
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::B_Q));
+        }
 
         // Closes a batch of `nslots` tiles: their row sums, rescaled to the running
         // max m_now, go into l and (warpgroup 0, V-Smooth) into the bf16 A operand
@@ -645,7 +685,7 @@ bool make_map_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t ro
 }
 
 template <int D, bool E, bool S, bool G>
-vc_status launch_one(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const AttnParams& p,
+vc_status launch_one(const CUtensorMap& mk, const CUtensorMap& mv, const AttnParams& p,
                      dim3 grid, cudaStream_t st) {
     auto kern = attn_fwd_kernel<D, E, S, G>;
     static bool attr = false;
@@ -654,25 +694,25 @@ vc_status launch_one(const CUtensorMap& mq, const CUtensorMap& mk, const CUtenso
         if (e != cudaSuccess) return cuda_status(e);
         attr = true;
     }
-    kern<<<grid, kThreads, Cfg<D>::SMEM, st>>>(mq, mk, mv, p);
+    kern<<<grid, kThreads, Cfg<D>::SMEM, st>>>(mk, mv, p);
     return cuda_status(cudaGetLastError());
 }
 
 template <int D>
-vc_status launch_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const AttnParams& p,
+vc_status launch_d(const CUtensorMap& mk, const CUtensorMap& mv, const AttnParams& p,
                    dim3 grid, cudaStream_t st, int expcast, int vsmooth, bool dbg) {
     if (dbg) {
         if (expcast)
-            return vsmooth ? launch_one<D, true, true, true>(mq, mk, mv, p, grid, st)
-                           : launch_one<D, true, false, true>(mq, mk, mv, p, grid, st);
-        return vsmooth ? launch_one<D, false, true, true>(mq, mk, mv, p, grid, st)
-                       : launch_one<D, false, false, true>(mq, mk, mv, p, grid, st);
+            return vsmooth ? launch_one<D, true, true, true>(mk, mv, p, grid, st)
+                           : launch_one<D, true, false, true>(mk, mv, p, grid, st);
+        return vsmooth ? launch_one<D, false, true, true>(mk, mv, p, grid, st)
+                       : launch_one<D, false, false, true>(mk, mv, p, grid, st);
     }
     if (expcast)
-        return vsmooth ? launch_one<D, true, true, false>(mq, mk, mv, p, grid, st)
-                       : launch_one<D, true, false, false>(mq, mk, mv, p, grid, st);
-    return vsmooth ? launch_one<D, false, true, false>(mq, mk, mv, p, grid, st)
-                   : launch_one<D, false, false, false>(mq, mk, mv, p, grid, st);
+        return vsmooth ? launch_one<D, true, true, false>(mk, mv, p, grid, st)
+                       : launch_one<D, true, false, false>(mk, mv, p, grid, st);
+    return vsmooth ? launch_one<D, false, true, false>(mk, mv, p, grid, st)
+                   : launch_one<D, false, false, false>(mk, mv, p, grid, st);
 }
 
 }  // namespace
@@ -684,13 +724,13 @@ vc_status launch_attn(const uint8_t* Q8, const float* sq, const uint8_t* K8, con
     const int64_t Npad = npad_of(s.N);
     const uint64_t rows_qk = (uint64_t)s.B * s.H * Npad;
     const uint64_t rows_v = (uint64_t)s.B * s.H * s.d;
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mk, mv;
     const CUtensorMapSwizzle qk_swz = (s.d == 128) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-    if (!make_map_2d(&mq, Q8, s.d, rows_qk, s.d, s.d, 128, qk_swz) ||
-        !make_map_2d(&mk, K8, s.d, rows_qk, s.d, s.d, 128, qk_swz) ||
+    if (!make_map_2d(&mk, K8, s.d, rows_qk, s.d, s.d, 128, qk_swz) ||
         !make_map_2d(&mv, V8T, Npad, rows_v, Npad, 128, s.d, CU_TENSOR_MAP_SWIZZLE_128B))
         return VC_ERR_CUDA;
     AttnParams p{};
+    p.Q8 = Q8;
     p.sq = sq;
     p.sk = sk;
     p.sv = sv;
@@ -712,8 +752,8 @@ vc_status launch_attn(const uint8_t* Q8, const float* sq, const uint8_t* K8, con
     p.S_dump = dbg ? dbg->S : nullptr;
     p.P_dump = dbg ? dbg->P : nullptr;
     const dim3 grid(nblk, s.H, s.B);
-    if (s.d == 128) return launch_d<128>(mq, mk, mv, p, grid, st, expcast, vsmooth, dbg != nullptr);
-    return launch_d<64>(mq, mk, mv, p, grid, st, expcast, vsmooth, dbg != nullptr);
+    if (s.d == 128) return launch_d<128>(mk, mv, p, grid, st, expcast, vsmooth, dbg != nullptr);
+    return launch_d<64>(mk, mv, p, grid, st, expcast, vsmooth, dbg != nullptr);
 }
 
 }  // namespace vc

@@ -37,6 +37,30 @@ def _small(N=300, d=64, H=2, seed=5):
     return inputs.to_u16(Q), inputs.to_u16(K), inputs.to_u16(V)
 
 
+def test_mean_restore_identity(oracle_mod):
+    """P (R + 1 mu_j) = P R + r_ij mu_j ([R] step 3; dimensionstp.github.io, 2-3).
+
+    With every row's maximum planted in the first tile no rescale ever happens,
+    so the oracle's output (which adds r_ij mu_j per tile) must equal the fp64
+    weighted mean of the dequantized V' = s_v R_q + mu_j under its own bytes.
+    A dropped mean term, a wrong block index or a wrong channel scale fails.
+    """
+    N, d = 700, 64
+    Q, K, V = _small(N=N, d=d, seed=21)
+    qz = oracle_mod.quantize(Q, K, V, None, 1)
+    B, H, Npad, _ = qz["Q8"].shape
+    rng = np.random.default_rng(3)
+    rows = np.arange(0, N, 7, dtype=np.int32)
+    acc = rng.normal(0.0, 20.0, (B, H, rows.size, Npad)).astype(np.float32)
+    acc[..., 0] = 200.0   # the running max is fixed by tile 0
+    O, P = oracle_mod.attn(qz, N, softmax_scale=LN2, rows=rows, acc_in=acc, want_codes=True)
+    w = oracle_mod.e4m3_decode(P)                     # [B,H,nrows,Npad]
+    v = _dequant_v(oracle_mod, qz, 1)                 # [B,H,Npad,d]
+    want = np.einsum("bhrt,bhtd->bhrd", w, v) / w.sum(axis=-1, keepdims=True)
+    assert np.all(w[..., N:] == 0)
+    np.testing.assert_allclose(O, want, rtol=1e-10, atol=1e-12)
+
+
 def test_reference_permutation_identity(oracle_mod):
     Q, K, V = _small(N=260)
     rng = np.random.default_rng(0)

@@ -390,6 +390,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             };
             bool ok = mbar_wait_warp(bar(C::B_Q), 0, abort_flag, p.dev_status, tmo);
+            // tile B starts half a step behind tile A
+            if (X == 1 && ok) ok = mbar_wait_warp(bar(C::B_PF + 0), 0, abort_flag, p.dev_status, tmo);
             for (int j = 0; ok && j < J; ++j) {
                 if (j > 0) {
                     // S_X free: the softmax has read the row sum of tile j-1 back

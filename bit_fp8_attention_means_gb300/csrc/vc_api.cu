@@ -53,7 +53,7 @@ vc_status vc_cluster(const void* V, vc_shape shape, int k, int iters, int warm_s
     vc_status st = check_shape(shape);
     if (st != VC_OK) return st;
     if (!V || !centroids || !labels || !perm) return VC_ERR_INVALID_ARG;
-    if (!aligned16(V)) return VC_ERR_INVALID_ARG;
+    if (!aligned16(V) || !aligned16(centroids)) return VC_ERR_INVALID_ARG;
     if (iters < 1 || (warm_start != 0 && warm_start != 1)) return VC_ERR_INVALID_ARG;
     if (k < 1 || k > 1024) return VC_ERR_UNSUPPORTED;
     if (k > shape.N) return VC_ERR_INVALID_ARG;

@@ -136,19 +136,6 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
     asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
 
-__device__ __forceinline__ void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-// Bounded wait that ignores the abort flag: used at teardown to let this
-// CTA's own copies and MMAs in flight finish before their memory is released.
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t timeout_ns) {
-    const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(bar, parity)) {
-        if (globaltimer_ns() - t0 > timeout_ns) return;
-    }
-}
-
 // Byte offset of element (n, k) of a 48-deep bf16 operand buffer: K-major, no
 // swizzle, core matrices of 8 rows x 8 bf16 (16 bytes), 6 along K per group of
 // 8 rows.
@@ -657,21 +644,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ------------------------------------------------------------------ host side
 
-// cuTensorMapEncodeTiled is a driver API; it is looked up through the runtime
-// so that the library does not link against libcuda directly.
-PFN_cuTensorMapEncodeTiled_v12000 encode_tiled_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        void* ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    }
-    return fn;
-}
-
 bool make_map_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t row_bytes,
                  uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swz) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_tiled_fn();
@@ -718,6 +690,19 @@ vc_status launch_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorM
 }
 
 }  // namespace
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_tiled_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
 
 vc_status launch_attn(const uint8_t* Q8, const float* sq, const uint8_t* K8, const float* sk, const uint8_t* V8T,
                       const float* sv, const uint16_t* mu, const vc_shape& s, float softmax_scale, int expcast,

@@ -18,6 +18,10 @@
 //   update_kernel    centroid i = fp32 mean of its members, read contiguously
 //                    through pi; empty clusters keep their centroid.
 // Labels and pi of the last assignment are the outputs.
+#include <algorithm>
+
+#include <cuda_bf16.h>
+
 #include "vc_device.cuh"
 #include "vc_internal.h"
 
@@ -255,27 +259,269 @@ __global__ void seg_scatter(const int32_t* labels, int N, int k, int nseg, const
     }
 }
 
-// Centroid i = mean of its members (fp32 sum through pi); empty keeps the old value.
+// Centroid i = mean of its members (fp32 sums through pi); empty keeps the old
+// value.  A CTA per (centroid, head): D/8 lanes each own 8 channels (one
+// 16-byte load per member row), 256/(D/8) member groups stride over the
+// members, then the groups' partial sums are added in shared memory.
+constexpr int kUpdThreads = 256;
+
 template <int D>
-__global__ void __launch_bounds__(D) update_kernel(const uint16_t* V, vc_shape s, int k, const int32_t* perm,
-                                                   const int32_t* count, const int32_t* start, float* cent) {
-    const int i = blockIdx.x, bh = blockIdx.y, b = bh / s.H, h = bh % s.H, c = threadIdx.x;
+__global__ void __launch_bounds__(kUpdThreads) update_kernel(const uint16_t* V, vc_shape s, int k,
+                                                             const int32_t* perm, const int32_t* count,
+                                                             const int32_t* start, float* cent) {
+    constexpr int LANES = D / 8;
+    constexpr int GROUPS = kUpdThreads / LANES;
+    __shared__ float red[GROUPS][D];
+    const int i = blockIdx.x, bh = blockIdx.y, b = bh / s.H, h = bh % s.H;
     const int n = count[(int64_t)bh * k + i];
     if (n == 0) return;
     const int st = start[(int64_t)bh * k + i];
     const int32_t* p = perm + (int64_t)bh * s.N + st;
-    float acc = 0.f;
-    int e = 0;
-    for (; e + 4 <= n; e += 4) {
-        const int t0 = p[e], t1 = p[e + 1], t2 = p[e + 2], t3 = p[e + 3];
-        const float v0 = bf16_bits_to_f32(tok_ptr(V, s, b, h, t0)[c]);
-        const float v1 = bf16_bits_to_f32(tok_ptr(V, s, b, h, t1)[c]);
-        const float v2 = bf16_bits_to_f32(tok_ptr(V, s, b, h, t2)[c]);
-        const float v3 = bf16_bits_to_f32(tok_ptr(V, s, b, h, t3)[c]);
-        acc = __fadd_rn(__fadd_rn(acc, v0), __fadd_rn(v1, __fadd_rn(v2, v3)));
+    const int lane = threadIdx.x % LANES, grp = threadIdx.x / LANES;
+    float acc[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) acc[q] = 0.f;
+    auto add_row = [&](const uint4 w) {
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            acc[2 * q] = __fadd_rn(acc[2 * q], bf16_bits_to_f32(ws[q] & 0xFFFFu));
+            acc[2 * q + 1] = __fadd_rn(acc[2 * q + 1], bf16_bits_to_f32(ws[q] >> 16));
+        }
+    };
+    int e = grp;
+    for (; e + 3 * GROUPS < n; e += 4 * GROUPS) {
+        uint4 w[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            w[u] = __ldg(reinterpret_cast<const uint4*>(tok_ptr(V, s, b, h, __ldg(p + e + u * GROUPS)) + lane * 8));
+#pragma unroll
+        for (int u = 0; u < 4; ++u) add_row(w[u]);
     }
-    for (; e < n; ++e) acc = __fadd_rn(acc, bf16_bits_to_f32(tok_ptr(V, s, b, h, p[e])[c]));
-    cent[((int64_t)bh * k + i) * D + c] = __fdiv_rn(acc, (float)n);
+    for (; e < n; e += GROUPS)
+        add_row(__ldg(reinterpret_cast<const uint4*>(tok_ptr(V, s, b, h, __ldg(p + e)) + lane * 8)));
+#pragma unroll
+    for (int q = 0; q < 8; ++q) red[grp][lane * 8 + q] = acc[q];
+    __syncthreads();
+    for (int c = threadIdx.x; c < D; c += kUpdThreads) {
+        float sum = 0.f;
+#pragma unroll 8
+        for (int g = 0; g < GROUPS; ++g) sum = __fadd_rn(sum, red[g][c]);
+        cent[((int64_t)bh * k + i) * D + c] = __fdiv_rn(sum, (float)n);
+    }
+}
+
+// ------------------------------------------------------------ assignment on the tensor cores
+//
+// z_t = argmin_i (|c_i|^2 - 2 v_t . c_i) with v . c on tcgen05: A = a tile of
+// 128 tokens (bf16, exact), B = the centroids split into two bf16 parts
+// c = c_hi + c_lo (c_lo = bf16(c - c_hi); the pair keeps ~16 significant bits,
+// so |v . c - v . (c_hi + c_lo)| <= 2^-17 |v||c|), accumulated in fp32 in
+// TMEM; the epilogue adds |c|^2 (fp32, as centroid_norms) and takes the
+// argmin with ties to the lowest index.  Used for k <= 256.
+//
+// Persistent CTAs, each over a contiguous range of (head, token-tile) pairs;
+// a range spans few heads, and the centroids of a head are split into shared
+// memory once per head.  6 warps: warp 0 TMA producer (token tiles, 2
+// stages), warp 1 MMA issuer and TMEM owner (2 accumulators of 256 columns),
+// warps 2-5 epilogue (one TMEM lane quadrant each).
+constexpr int kAsThreads = 192;
+constexpr int kAsMaxK = 256;
+
+template <int D>
+struct AsCfg {
+    static constexpr int KBLK = D / 64;                 // 64-channel K blocks (128-byte swizzled rows)
+    static constexpr int TILE_BYTES = KBLK * 128 * 128; // one token tile
+    static constexpr int CPART = KBLK * kAsMaxK * 128;  // one centroid part
+    static constexpr int OFF_C = 0;                     // [2 parts]
+    static constexpr int OFF_V = OFF_C + 2 * CPART;     // [2 stages]
+    static constexpr int OFF_N = OFF_V + 2 * TILE_BYTES;  // |c|^2, kAsMaxK floats
+    static constexpr int OFF_BAR = OFF_N + kAsMaxK * 4;
+    static constexpr int OFF_MISC = OFF_BAR + 8 * 8;
+    static constexpr int SMEM = OFF_MISC + 64 + 1024;
+    static_assert(SMEM <= 232448, "shared memory budget");
+    // barriers: VF[2] tile loaded, VE[2] tile read, DF[2] accumulator ready, DE[2] accumulator read
+    static constexpr int B_VF = 0, B_VE = 2, B_DF = 4, B_DE = 6;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kAsThreads, 1)
+    assign_tc_kernel(const __grid_constant__ CUtensorMap tmV, vc_shape s, int k, int kpad, int tiles_per_head,
+                     int total, const float* cent, int32_t* labels, int32_t* dev_status, uint64_t tmo) {
+    using C = AsCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    auto bar = [&](int i) -> uint32_t { return sbase + C::OFF_BAR + 8u * (uint32_t)i; };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 16);
+    float* cn_s = reinterpret_cast<float*>(smem + C::OFF_N);
+    const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0), lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(C::B_VF + i), 1);
+            mbar_init(bar(C::B_VE + i), 1);
+            mbar_init(bar(C::B_DF + i), 1);
+            mbar_init(bar(C::B_DE + i), 4);
+        }
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = __shfl_sync(0xffffffffu, *tmem_slot, 0);
+
+    const int per = (total + gridDim.x - 1) / gridDim.x;
+    const int g0 = blockIdx.x * per, g1 = min(total, g0 + per);
+    const uint32_t idesc = idesc_bf16(128, (uint32_t)kpad);
+    int n = 0;  // tiles this CTA has processed (barrier phases)
+    bool ok = true;
+    for (int seg = g0; seg < g1 && ok;) {
+        const int bh = seg / tiles_per_head;
+        const int seg_end = min(g1, (bh + 1) * tiles_per_head);
+        const int b = bh / s.H, h = bh % s.H;
+        // ---- centroids of head bh: two bf16 parts in the 128-byte swizzled
+        // K-major layout of the B operand, and |c|^2
+        const float* cb = cent + (int64_t)bh * k * D;
+        for (int e = threadIdx.x; e < kpad * (D / 8); e += kAsThreads) {
+            const int c = e / (D / 8), kc = e % (D / 8);  // centroid, 8-channel chunk
+            float x[8];
+            if (c < k) {
+                const float4 x0 = *reinterpret_cast<const float4*>(cb + (int64_t)c * D + kc * 8);
+                const float4 x1 = *reinterpret_cast<const float4*>(cb + (int64_t)c * D + kc * 8 + 4);
+                x[0] = x0.x; x[1] = x0.y; x[2] = x0.z; x[3] = x0.w;
+                x[4] = x1.x; x[5] = x1.y; x[6] = x1.z; x[7] = x1.w;
+            } else {
+#pragma unroll
+                for (int q = 0; q < 8; ++q) x[q] = 0.f;
+            }
+            uint32_t hi[4], lo[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const __nv_bfloat16 h0 = __float2bfloat16_rn(x[2 * q]), h1 = __float2bfloat16_rn(x[2 * q + 1]);
+                const __nv_bfloat16 l0 = __float2bfloat16_rn(__fsub_rn(x[2 * q], __bfloat162float(h0)));
+                const __nv_bfloat16 l1 = __float2bfloat16_rn(__fsub_rn(x[2 * q + 1], __bfloat162float(h1)));
+                hi[q] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+                lo[q] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
+            }
+            const int kb = kc / 8, chunk = kc % 8;
+            const uint32_t off = kb * (kAsMaxK * 128) + (c >> 3) * 1024 + (c & 7) * 128 + ((chunk ^ (c & 7)) << 4);
+            *reinterpret_cast<uint4*>(smem + C::OFF_C + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<uint4*>(smem + C::OFF_C + C::CPART + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        }
+        for (int c = threadIdx.x; c < kpad; c += kAsThreads) {
+            float acc = 0.f;
+            if (c < k)
+                for (int e = 0; e < D; ++e) acc = __fmaf_rn(cb[(int64_t)c * D + e], cb[(int64_t)c * D + e], acc);
+            cn_s[c] = acc;
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        const int ntile = seg_end - seg;
+        if (warp == 0) {
+            // ---- producer: token tiles of this head
+            for (int i = 0; i < ntile; ++i) {
+                const int m = n + i, st = m & 1;
+                if (m >= 2 && !mbar_wait_warp(bar(C::B_VE + st), ((m >> 1) - 1) & 1, abort_flag, dev_status, tmo)) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) {
+                    const int t0 = (seg + i - bh * tiles_per_head) * 128;
+                    mbar_arrive_expect_tx(bar(C::B_VF + st), C::TILE_BYTES);
+#pragma unroll
+                    for (int kb = 0; kb < C::KBLK; ++kb)
+                        tma_load_4d(sbase + C::OFF_V + st * C::TILE_BYTES + kb * 16384, &tmV, kb * 64, h, t0, b,
+                                    bar(C::B_VF + st));
+                }
+                __syncwarp();
+            }
+        } else if (warp == 1) {
+            // ---- MMA issuer
+            for (int i = 0; i < ntile; ++i) {
+                const int m = n + i, st = m & 1, buf = m & 1;
+                if (!mbar_wait_warp(bar(C::B_VF + st), (m >> 1) & 1, abort_flag, dev_status, tmo) ||
+                    (m >= 2 && !mbar_wait_warp(bar(C::B_DE + buf), ((m >> 1) - 1) & 1, abort_flag, dev_status, tmo))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem + buf * 256;
+#pragma unroll
+                for (int part = 0; part < 2; ++part)
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const int kb = kk / 4, kin = (kk % 4) * 32;
+                        const uint64_t ad =
+                            smem_desc(sbase + C::OFF_V + st * C::TILE_BYTES + kb * 16384 + kin, 1024, kSwizzle128B);
+                        const uint64_t bd = smem_desc(sbase + C::OFF_C + part * C::CPART + kb * (kAsMaxK * 128) + kin,
+                                                      1024, kSwizzle128B);
+                        mma_bf16_ss_w(d_tmem, ad, bd, idesc, (part > 0 || kk > 0) ? 1u : 0u);
+                    }
+                mma_commit_w(bar(C::B_DF + buf));
+                mma_commit_w(bar(C::B_VE + st));
+            }
+        } else {
+            // ---- epilogue: argmin over the centroids for one token row
+            const int q = warp & 3, row = q * 32 + lane;
+            const uint32_t lane_addr = tmem + ((uint32_t)(q * 32) << 16);
+            for (int i = 0; i < ntile; ++i) {
+                const int m = n + i, buf = m & 1;
+                if (!mbar_wait_warp(bar(C::B_DF + buf), (m >> 1) & 1, abort_flag, dev_status, tmo)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                float best = INFINITY;
+                int arg = 0;
+                for (int c0 = 0; c0 < kpad; c0 += 16) {
+                    uint32_t r[16];
+                    tmem_ld16(lane_addr + buf * 256 + c0, r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const int c = c0 + e;
+                        const float dist = __fmaf_rn(-2.f, __uint_as_float(r[e]), cn_s[c]);
+                        if (c < k && dist < best) {
+                            best = dist;
+                            arg = c;
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(C::B_DE + buf));
+                const int t = (seg + i - bh * tiles_per_head) * 128 + row;
+                if (t < s.N) labels[(int64_t)bh * s.N + t] = arg;
+            }
+        }
+        // every role has finished this head's tiles (the epilogue waited for the
+        // last accumulator, so every MMA reading the centroid parts is complete)
+        n += ntile;
+        seg = seg_end;
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        ok = ok && (*abort_flag == 0);
+    }
+    // let the producer's copies in flight land before the CTA exits
+    if (warp == 0 && n > 0) {
+        for (int m = (n > 2 ? n - 2 : 0); m < n; ++m) drain_wait(bar(C::B_VF + (m & 1)), (m >> 1) & 1, tmo);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
 }
 
 }  // namespace
@@ -286,9 +532,23 @@ size_t cluster_workspace(const vc_shape& s, int k) {
     return align256(BH * k * 4) + align256(BH * nseg * k * 4) + align256(BH * k * 4) + align256(BH * k * 4);
 }
 
+// Tensor map over V [B, N, H, d] (bf16) for the assignment kernel: boxes of
+// 64 channels x 1 head x 128 tokens, 128-byte swizzled.
+static bool make_v_map(CUtensorMap* map, const uint16_t* V, const vc_shape& s) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_tiled_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[4] = {(cuuint64_t)s.d, (cuuint64_t)s.H, (cuuint64_t)s.N, (cuuint64_t)s.B};
+    const cuuint64_t strides[3] = {(cuuint64_t)s.s_h * 2, (cuuint64_t)s.s_n * 2, (cuuint64_t)s.s_b * 2};
+    const cuuint32_t box[4] = {64, 1, 128, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<uint16_t*>(V), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int D>
 static vc_status launch_cluster_d(const uint16_t* V, const vc_shape& s, int k, int iters, int warm, float* cent,
-                                  int32_t* labels, int32_t* perm, void* ws, cudaStream_t st) {
+                                  int32_t* labels, int32_t* perm, void* ws, int32_t* dev_status, cudaStream_t st) {
     const int BH = s.B * s.H;
     const int nseg = (s.N + kSeg - 1) / kSeg;
     ClusterWs w = carve(ws, s, k);
@@ -297,16 +557,34 @@ static vc_status launch_cluster_d(const uint16_t* V, const vc_shape& s, int k, i
     static bool attr_set = false;
     if (!attr_set) {
         cudaFuncSetAttribute(assign_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)assign_smem);
+        cudaFuncSetAttribute(assign_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, AsCfg<D>::SMEM);
         attr_set = true;
     }
+    const bool tc = k <= kAsMaxK;
+    CUtensorMap vmap;
+    int grid_tc = 0;
+    const int tiles_per_head = (s.N + 127) / 128;
+    if (tc) {
+        if (!make_v_map(&vmap, V, s)) return VC_ERR_CUDA;
+        int dev = 0, sms = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        grid_tc = (int)std::min<int64_t>((int64_t)BH * tiles_per_head, sms > 0 ? sms : 1);
+    }
+    const int kpad = (k + 15) & ~15;
     for (int it = 0; it < iters; ++it) {
-        centroid_norms<<<dim3((unsigned)((k + 127) / 128), BH), 128, 0, st>>>(cent, k, D, w.cnorm);
-        assign_kernel<D><<<dim3((s.N + kTokTile - 1) / kTokTile, BH), kAssignThreads, assign_smem, st>>>(
-            V, s, k, cent, w.cnorm, labels);
+        if (tc) {
+            assign_tc_kernel<D><<<grid_tc, kAsThreads, AsCfg<D>::SMEM, st>>>(
+                vmap, s, k, kpad, tiles_per_head, BH * tiles_per_head, cent, labels, dev_status, 4000000000ull);
+        } else {
+            centroid_norms<<<dim3((unsigned)((k + 127) / 128), BH), 128, 0, st>>>(cent, k, D, w.cnorm);
+            assign_kernel<D><<<dim3((s.N + kTokTile - 1) / kTokTile, BH), kAssignThreads, assign_smem, st>>>(
+                V, s, k, cent, w.cnorm, labels);
+        }
         seg_hist<<<dim3(nseg, BH), 256, k * 4, st>>>(labels, s.N, k, nseg, w.seg);
         seg_scan<<<BH, 256, 0, st>>>(k, nseg, w.seg, w.count, w.start);
         seg_scatter<<<dim3(nseg, BH), 32, k * 4, st>>>(labels, s.N, k, nseg, w.seg, perm);
-        update_kernel<D><<<dim3(k, BH), D, 0, st>>>(V, s, k, perm, w.count, w.start, cent);
+        update_kernel<D><<<dim3(k, BH), kUpdThreads, 0, st>>>(V, s, k, perm, w.count, w.start, cent);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return cuda_status(e);
     }
@@ -315,9 +593,8 @@ static vc_status launch_cluster_d(const uint16_t* V, const vc_shape& s, int k, i
 
 vc_status launch_cluster(const uint16_t* V, const vc_shape& s, int k, int iters, int warm, float* cent,
                          int32_t* labels, int32_t* perm, void* ws, int32_t* dev_status, cudaStream_t st) {
-    (void)dev_status;  // no device-side waits in these kernels
-    if (s.d == 128) return launch_cluster_d<128>(V, s, k, iters, warm, cent, labels, perm, ws, st);
-    return launch_cluster_d<64>(V, s, k, iters, warm, cent, labels, perm, ws, st);
+    if (s.d == 128) return launch_cluster_d<128>(V, s, k, iters, warm, cent, labels, perm, ws, dev_status, st);
+    return launch_cluster_d<64>(V, s, k, iters, warm, cent, labels, perm, ws, dev_status, st);
 }
 
 }  // namespace vc

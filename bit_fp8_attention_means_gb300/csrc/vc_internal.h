@@ -2,6 +2,7 @@
 #pragma once
 #include <cstdint>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include "vc.h"
 
@@ -14,6 +15,10 @@ inline int64_t npad_of(int N) { return (int64_t)nblk_of(N) * kBlock; }
 
 vc_status check_shape(const vc_shape& s);
 vc_status cuda_status(cudaError_t e);
+
+// cuTensorMapEncodeTiled, looked up through the runtime so that the library
+// does not link against the driver library directly; null if unavailable.
+PFN_cuTensorMapEncodeTiled_v12000 encode_tiled_fn();
 
 // quantizer (vc_quantize.cu)
 size_t quantize_workspace(const vc_shape& s);

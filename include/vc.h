@@ -85,7 +85,8 @@ int vc_version(void);
  *              centroid.
  *   warm_start 1: start from `centroids` as given (previous step's state);
  *              0: centroid i starts at token floor(i*N/k).
- *   centroids  fp32 [B,H,k,d], in/out (the warm-start state the caller keeps).
+ *   centroids  fp32 [B,H,k,d], in/out (the warm-start state the caller keeps),
+ *              16-byte aligned.
  *   labels     int32 [B,H,N], out: label of every token from the last
  *              assignment (the centroids are the means of these groups).
  *   perm       int32 [B,H,N], out: pi, the stable argsort of labels (ascending
@@ -93,8 +94,17 @@ int vc_version(void);
  *              token perm[t].
  *   workspace  device scratch of at least vc_cluster_workspace(shape, k) bytes,
  *              256-byte aligned; contents on entry are ignored.
- * Label choice between near-equidistant centroids follows fp32 rounding and
- * is not guaranteed to be bit-reproducible across hardware.
+ *   dev_status nullable device int32; a device-side wait that gives up writes
+ *              VC_ERR_TIMEOUT there.
+ * The distances are |c|^2 - 2 v.c.  For k <= 256 the products v.c run on the
+ * tensor cores with each centroid split into two bf16 parts (about 16
+ * significant bits, |error| <= 2^-17 |v||c|) and fp32 accumulation; for
+ * larger k they are fp32 on the CUDA cores.  Label choice between
+ * near-equidistant centroids therefore follows that rounding and is not
+ * guaranteed to be bit-reproducible across hardware.
+ * Errors: VC_ERR_INVALID_ARG (null or misaligned pointers, iters < 1, k > N),
+ * VC_ERR_UNSUPPORTED (k outside 1..1024, d not 64 or 128), VC_ERR_WORKSPACE,
+ * VC_ERR_CUDA (launch failure).
  */
 size_t vc_cluster_workspace(vc_shape shape, int k);
 vc_status vc_cluster(const void* V, vc_shape shape, int k, int iters, int warm_start,

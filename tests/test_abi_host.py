@@ -86,6 +86,8 @@ def test_quantize_and_cluster_argument_errors(L):
     assert L.vc_cluster(FAKE, s, 2000, 1, 0, FAKE, FAKE, FAKE, FAKE, cw, None, None) == 2
     assert L.vc_cluster(FAKE, s, 8, 0, 0, FAKE, FAKE, FAKE, FAKE, cw, None, None) == 1
     assert L.vc_cluster(FAKE, s, 8, 1, 0, FAKE, FAKE, FAKE, FAKE, cw - 1, None, None) == 3
+    unaligned = ctypes.c_void_p(0x10008)
+    assert L.vc_cluster(FAKE, s, 8, 1, 0, unaligned, FAKE, FAKE, FAKE, cw, None, None) == 1
     small = _shape(N=4)
     assert L.vc_cluster(FAKE, small, 8, 1, 0, FAKE, FAKE, FAKE, FAKE, 1 << 20, None, None) == 1
     assert L.vc_debug_wait_timeout(None, 10, None) == 1

@@ -12,6 +12,8 @@
 //   quant_v_codes_kernel residual codes, written token-contiguous per channel
 //                        (V8T [B,H,d,Npad]) so that the attention kernel can
 //                        read V as a K-major MMA operand.
+// The two V kernels stage each block's gathered rows in shared memory with
+// 16-byte loads; the per-channel scale needs the whole head, hence two passes.
 // Every rounding step is written with an explicit _rn intrinsic so that the
 // codes are bit-reproducible: fp32 block sum in token order, IEEE division,
 // round-to-nearest-even conversions (cvt.rn.satfinite.e4m3x2).
@@ -110,70 +112,100 @@ struct VArgs {
     float* sv;          // [B,H,D]
 };
 
-// Loads the block's 128 rows of channel c of V' (gathered) into registers.
+constexpr int kVThreads = 256;
+
+// Stages the block's rows of V' (gathered through pi) into shared memory as
+// bf16 [128][D] with 16-byte loads; rows beyond the valid count are zero.
+// Returns the number of valid rows.
 template <int D>
-__device__ __forceinline__ int load_v_column(const VArgs& a, int b, int h, int j, int c, float (&v)[kBlock],
-                                             int32_t* src_s) {
+__device__ __forceinline__ int stage_v_block(const VArgs& a, int b, int h, int j, uint16_t* vs, int32_t* src_s) {
     const int bh = b * a.H + h;
     const int t0 = j * kBlock;
     const int cnt = min(kBlock, a.N - t0);
-    for (int i = threadIdx.x; i < kBlock; i += blockDim.x)
+    if (threadIdx.x < kBlock) {
+        const int i = threadIdx.x;
         src_s[i] = (i < cnt) ? (a.perm ? __ldg(a.perm + (int64_t)bh * a.N + t0 + i) : t0 + i) : 0;
-    __syncthreads();
-    const uint16_t* base = a.V + (int64_t)b * a.s_b + (int64_t)h * a.s_h + c;
-#pragma unroll
-    for (int i = 0; i < kBlock; ++i) {
-        v[i] = (i < cnt) ? bf16_bits_to_f32(__ldg(base + (int64_t)src_s[i] * a.s_n)) : 0.f;
     }
+    __syncthreads();
+    const uint16_t* base = a.V + (int64_t)b * a.s_b + (int64_t)h * a.s_h;
+    constexpr int CH = D / 8;  // 16-byte chunks per row
+#pragma unroll 4
+    for (int e = threadIdx.x; e < kBlock * CH; e += kVThreads) {
+        const int t = e / CH, q = e % CH;
+        uint4 w = make_uint4(0, 0, 0, 0);
+        if (t < cnt) w = __ldg(reinterpret_cast<const uint4*>(base + (int64_t)src_s[t] * a.s_n) + q);
+        *reinterpret_cast<uint4*>(vs + t * D + q * 8) = w;
+    }
+    __syncthreads();
     return cnt;
 }
 
+// Block means (fp32 sum in token order, one thread per channel) and the
+// per-channel maximum of |V' - mu| (atomicMax on the fp32 bit pattern, values
+// are >= 0).  One CTA per (block, head, batch).
 template <int D>
-__global__ void __launch_bounds__(D) quant_v_stats_kernel(VArgs a) {
+__global__ void __launch_bounds__(kVThreads) quant_v_stats_kernel(VArgs a) {
+    __shared__ __align__(16) uint16_t vs[kBlock * D];
     __shared__ int32_t src_s[kBlock];
-    const int b = blockIdx.z, h = blockIdx.y, j = blockIdx.x, c = threadIdx.x;
+    __shared__ float mu_s[D];
+    __shared__ float part_s[kVThreads];
+    const int b = blockIdx.z, h = blockIdx.y, j = blockIdx.x;
     const int bh = b * a.H + h;
-    float v[kBlock];
-    const int cnt = load_v_column<D>(a, b, h, j, c, v, src_s);
-    float m = 0.f;
-    if (a.vsmooth) {
-        float sum = 0.f;
-#pragma unroll
-        for (int i = 0; i < kBlock; ++i)
-            if (i < cnt) sum = __fadd_rn(sum, v[i]);
-        const __nv_bfloat16 mb = __float2bfloat16_rn(__fdiv_rn(sum, (float)cnt));
-        const uint16_t bits = __bfloat16_as_ushort(mb);
-        a.mu[((int64_t)bh * a.nblk + j) * D + c] = bits;
-        m = bf16_bits_to_f32(bits);
+    const int cnt = stage_v_block<D>(a, b, h, j, vs, src_s);
+    if (threadIdx.x < D) {
+        const int c = threadIdx.x;
+        float m = 0.f;
+        if (a.vsmooth) {
+            float sum = 0.f;
+            for (int i = 0; i < cnt; ++i) sum = __fadd_rn(sum, bf16_bits_to_f32(vs[i * D + c]));
+            const uint16_t bits = __bfloat16_as_ushort(__float2bfloat16_rn(__fdiv_rn(sum, (float)cnt)));
+            a.mu[((int64_t)bh * a.nblk + j) * D + c] = bits;
+            m = bf16_bits_to_f32(bits);
+        }
+        mu_s[c] = m;
     }
+    __syncthreads();
+    constexpr int PARTS = kVThreads / D;
+    const int c = threadIdx.x % D, part = threadIdx.x / D;
+    const float m = mu_s[c];
     float amax = 0.f;
-#pragma unroll
-    for (int i = 0; i < kBlock; ++i)
-        if (i < cnt) amax = fmaxf(amax, fabsf(__fsub_rn(v[i], m)));
-    atomicMax(a.amax_ws + (int64_t)bh * D + c, __float_as_uint(amax));
+    for (int i = part; i < cnt; i += PARTS) amax = fmaxf(amax, fabsf(__fsub_rn(bf16_bits_to_f32(vs[i * D + c]), m)));
+    part_s[threadIdx.x] = amax;
+    __syncthreads();
+    if (threadIdx.x < D) {
+        for (int p2 = 1; p2 < PARTS; ++p2) amax = fmaxf(amax, part_s[p2 * D + c]);
+        atomicMax(a.amax_ws + (int64_t)bh * D + c, __float_as_uint(amax));
+    }
 }
 
+// Residual codes, written token-contiguous per channel (V8T [B,H,D,Npad]).
+// Thread (c, part) converts the block's tokens [part*T, part*T + T) of channel c.
 template <int D>
-__global__ void __launch_bounds__(D) quant_v_codes_kernel(VArgs a) {
+__global__ void __launch_bounds__(kVThreads) quant_v_codes_kernel(VArgs a) {
+    __shared__ __align__(16) uint16_t vs[kBlock * D];
     __shared__ int32_t src_s[kBlock];
-    const int b = blockIdx.z, h = blockIdx.y, j = blockIdx.x, c = threadIdx.x;
+    const int b = blockIdx.z, h = blockIdx.y, j = blockIdx.x;
     const int bh = b * a.H + h;
-    float v[kBlock];
-    const int cnt = load_v_column<D>(a, b, h, j, c, v, src_s);
+    const int cnt = stage_v_block<D>(a, b, h, j, vs, src_s);
+    constexpr int PARTS = kVThreads / D;
+    constexpr int T = kBlock / PARTS;  // tokens per thread
+    const int c = threadIdx.x % D, part = threadIdx.x / D;
     const float m = a.vsmooth ? bf16_bits_to_f32(a.mu[((int64_t)bh * a.nblk + j) * D + c]) : 0.f;
     const float amax = __uint_as_float(a.amax_ws[(int64_t)bh * D + c]);
     const float inv = amax > 0.f ? __fdiv_rn(448.f, amax) : 0.f;
-    if (j == 0) a.sv[(int64_t)bh * D + c] = __fdiv_rn(amax, 448.f);
-    uint4* out = reinterpret_cast<uint4*>(a.V8T + ((int64_t)bh * D + c) * a.Npad + (int64_t)j * kBlock);
+    if (j == 0 && part == 0) a.sv[(int64_t)bh * D + c] = __fdiv_rn(amax, 448.f);
+    uint4* out =
+        reinterpret_cast<uint4*>(a.V8T + ((int64_t)bh * D + c) * a.Npad + (int64_t)j * kBlock + part * T);
 #pragma unroll
-    for (int g = 0; g < kBlock / 16; ++g) {
+    for (int g = 0; g < T / 16; ++g) {
         uint32_t w[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            const int i = g * 16 + 4 * e;
+            const int i = part * T + g * 16 + 4 * e;
             float r[4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) r[u] = (i + u < cnt) ? __fmul_rn(__fsub_rn(v[i + u], m), inv) : 0.f;
+            for (int u = 0; u < 4; ++u)
+                r[u] = (i + u < cnt) ? __fmul_rn(__fsub_rn(bf16_bits_to_f32(vs[(i + u) * D + c]), m), inv) : 0.f;
             w[e] = cvt_e4m3x2(r[0], r[1]) | (cvt_e4m3x2(r[2], r[3]) << 16);
         }
         out[g] = make_uint4(w[0], w[1], w[2], w[3]);
@@ -199,10 +231,10 @@ static vc_status launch_quantize_d(const uint16_t* Q, const uint16_t* K, const u
     e = cudaMemsetAsync(amax_ws, 0, quantize_workspace(s), st);
     if (e != cudaSuccess) return cuda_status(e);
     VArgs va{V, s.s_b, s.s_n, s.s_h, perm, s.H, s.N, nblk, Npad, vsmooth, mu, amax_ws, V8T, sv};
-    quant_v_stats_kernel<D><<<dim3(nblk, s.H, s.B), D, 0, st>>>(va);
+    quant_v_stats_kernel<D><<<dim3(nblk, s.H, s.B), kVThreads, 0, st>>>(va);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_status(e);
-    quant_v_codes_kernel<D><<<dim3(nblk, s.H, s.B), D, 0, st>>>(va);
+    quant_v_codes_kernel<D><<<dim3(nblk, s.H, s.B), kVThreads, 0, st>>>(va);
     return cuda_status(cudaGetLastError());
 }
 

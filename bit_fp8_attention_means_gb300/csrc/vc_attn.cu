@@ -379,6 +379,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = mbar_wait_warp(bar(C::B_Q), 0, abort_flag, p.dev_status, tmo);
             // tile B starts half a step behind tile A
             if (X == 1 && ok) ok = mbar_wait_warp(bar(C::B_PF + 0), 0, abort_flag, p.dev_status, tmo);
+            // The waits for data that is normally already there (the K stage of the
+            // next tile, the V stage of this one) sit where this warp would idle
+            // anyway, so that after a softmax hand-off only the MMA issue remains.
+            ok = ok && mbar_wait_warp(bar(C::B_KF), 0, abort_flag, p.dev_status, tmo);
             for (int j = 0; ok && j < J; ++j) {
                 if (j > 0) {
                     // S_X free: the softmax has read the row sum of tile j-1 back
@@ -386,19 +390,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
-                    tc_fence_after();
-                    if (VSMOOTH && (j - 1) % kBatch == kBatch - 1) issue_mean((j - 1) / kBatch);
-                }
-                if (!mbar_wait_warp(bar(C::B_KF + j % NSK), (j / NSK) & 1, abort_flag, p.dev_status, tmo)) {
-                    ok = false;
-                    break;
+                    if (VSMOOTH && (j - 1) % kBatch == kBatch - 1) {
+                        tc_fence_after();
+                        issue_mean((j - 1) / kBatch);
+                    }
                 }
                 tc_fence_after();
                 issue_qk(j);
                 mma_commit_w(bar(C::B_SF + X));
                 mma_commit_w(bar(C::B_KE + j % NSK));
-                if (!mbar_wait_warp(bar(C::B_PF + X), j & 1, abort_flag, p.dev_status, tmo) ||
-                    !mbar_wait_warp(bar(C::B_VF + j % NSV), (j / NSV) & 1, abort_flag, p.dev_status, tmo)) {
+                if (!mbar_wait_warp(bar(C::B_VF + j % NSV), (j / NSV) & 1, abort_flag, p.dev_status, tmo) ||
+                    !mbar_wait_warp(bar(C::B_PF + X), j & 1, abort_flag, p.dev_status, tmo)) {
                     ok = false;
                     break;
                 }
@@ -406,6 +408,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 issue_pv(j);
                 mma_commit_w(bar(C::B_OD + X));
                 mma_commit_w(bar(C::B_VE + j % NSV));
+                if (j + 1 < J &&
+                    !mbar_wait_warp(bar(C::B_KF + (j + 1) % NSK), ((j + 1) / NSK) & 1, abort_flag, p.dev_status, tmo)) {
+                    ok = false;
+                    break;
+                }
             }
             if (ok && mbar_wait_warp(bar(C::B_SE + X), (J - 1) & 1, abort_flag, p.dev_status, tmo)) {
                 tc_fence_after();

@@ -18,6 +18,11 @@ activations, which are not available; these stand in for them):
 * ``sweep``  B=1 H=24 d=128 N in {4096,...,131072}, generated like ``wan``,
   k = N/512.
 
+Rotary tables (``rope_table``): (cos, sin) of the angle pos_a * base^(-2i/D_a)
+for each channel pair, with the pairs split over the three axes of a
+(frames, height, width) latent grid -- 21 x 45 x 80 = 75,600 tokens for the
+``wan`` shape -- or over one token axis when no grid is given.  base = 10^4.
+
 N(mu, v) denotes variance v.  Cluster memberships are i.i.d. uniform over
 token positions (no spatial locality), so a block in sequence order holds a
 mixture of clusters.  Tensors are bf16 in the layout [B, N, H, d].
@@ -26,7 +31,9 @@ from dataclasses import dataclass
 
 import torch
 
-__all__ = ["Workload", "WORKLOADS", "make_qkv", "drift_v", "sweep_workload"]
+__all__ = ["Workload", "WORKLOADS", "make_qkv", "drift_v", "sweep_workload", "rope_table", "WAN_GRID"]
+
+WAN_GRID = (21, 45, 80)  # latent frames x height x width of the 75,600-token shape
 
 
 @dataclass(frozen=True)
@@ -116,3 +123,31 @@ def drift_v(V: torch.Tensor, step: int, seed: int, var: float = 0.05) -> torch.T
 def to_u16(t: torch.Tensor):
     """bf16 tensor -> numpy uint16 bit patterns (CPU copy), same shape."""
     return t.detach().to("cpu").contiguous().view(torch.int16).numpy().view("uint16")
+
+
+def rope_table(N: int, d: int, grid=None, base: float = 10000.0):
+    """fp32 [N, d/2, 2]: (cos, sin) of the rotary angle of each token and
+    channel pair -- the memory layout of a complex64 [N, d/2] table.
+
+    With ``grid = (F, Hh, Ww)`` (F*Hh*Ww = N, token n at frame n // (Hh*Ww),
+    row (n // Ww) % Hh, column n % Ww) the d/2 pairs are split into
+    d/2 - 2*(d/2 // 3) frame pairs and d/2 // 3 pairs for each spatial axis;
+    otherwise all pairs follow the token index.
+    """
+    import numpy as np
+    half = d // 2
+    n = np.arange(N, dtype=np.int64)
+    if grid is None:
+        axes = [(n, half)]
+    else:
+        F, Hh, Ww = grid
+        assert F * Hh * Ww == N, (grid, N)
+        ps = half // 3
+        axes = [(n // (Hh * Ww), half - 2 * ps), ((n // Ww) % Hh, ps), (n % Ww, ps)]
+    ang = []
+    for pos, pairs in axes:
+        dim = 2 * pairs
+        omega = base ** (-np.arange(0, dim, 2, dtype=np.float64) / dim)
+        ang.append(np.outer(pos.astype(np.float64), omega))
+    a = np.concatenate(ang, axis=1)
+    return np.ascontiguousarray(np.stack([np.cos(a), np.sin(a)], axis=-1).astype(np.float32))

@@ -60,6 +60,12 @@ def lib():
         L.vco_quantize.argtypes = [_u16p, _u16p, _u16p, _int, _int, _int, _int, _i64, _i64, _i64,
                                    ctypes.c_void_p, _int, _u8p, _f32p, _u8p, _f32p, _u8p, _f32p,
                                    ctypes.c_void_p]
+        L.vco_quantize_ex.restype = _int
+        L.vco_quantize_ex.argtypes = [_u16p, _u16p, _u16p, _int, _int, _int, _int, _i64, _i64, _i64,
+                                      ctypes.c_void_p, _int, ctypes.c_void_p, _int,
+                                      _u8p, _f32p, _u8p, _f32p, _u8p, _f32p, ctypes.c_void_p]
+        L.vco_preproc_rows.restype = _int
+        L.vco_preproc_rows.argtypes = [_u16p, _i64, _int, ctypes.c_void_p, ctypes.c_void_p, _int, _f32p]
         L.vco_attn.restype = _int
         L.vco_attn.argtypes = [_u8p, _f32p, _u8p, _f32p, _u8p, _f32p, ctypes.c_void_p,
                                _int, _int, _int, _int, ctypes.c_float, _int, _int,
@@ -154,7 +160,35 @@ def argsort_labels(labels, k: int) -> np.ndarray:
     return perm
 
 
-def quantize(Q, K, V, perm=None, vsmooth: int = 1):
+def _rope_table(rope, N: int, d: int):
+    """fp32 [N, d/2, 2] (cos, sin) table -> (array kept alive, pointer)."""
+    if rope is None:
+        return None, None
+    r = np.ascontiguousarray(rope, dtype=np.float32)
+    assert r.shape == (N, d // 2, 2), r.shape
+    return r, r.ctypes.data_as(ctypes.c_void_p)
+
+
+def preproc_rows(X, pos=None, rope=None, hadamard: int = 0) -> np.ndarray:
+    """Rotary transform (row r at position pos[r]) then Hadamard rotation of
+    bf16 rows X [n, d]; returns the fp32 rows the Q/K quantizer encodes."""
+    X = np.ascontiguousarray(X, dtype=np.uint16)
+    n, d = X.shape
+    out = np.zeros((n, d), np.float32)
+    pp = None
+    if pos is not None:
+        pos = np.ascontiguousarray(pos, dtype=np.int32)
+        pp = pos.ctypes.data_as(ctypes.c_void_p)
+    r = np.ascontiguousarray(rope, dtype=np.float32) if rope is not None else None
+    rp = r.ctypes.data_as(ctypes.c_void_p) if r is not None else None
+    assert lib().vco_preproc_rows(X, n, d, pp, rp, int(hadamard), out) == 0
+    return out
+
+
+def quantize(Q, K, V, perm=None, vsmooth: int = 1, rope=None, hadamard: int = 0):
+    """Q/K/V quantizer.  With ``rope`` (fp32 [N, d/2, 2]) and/or ``hadamard``
+    the Q and K rows are rotated / Hadamard-transformed before quantization
+    and sq carries the factor 1/d."""
     Q, (sb, sn, sh) = _bnhd(Q)
     K, _ = _bnhd(K)
     V, _ = _bnhd(V)
@@ -170,9 +204,10 @@ def quantize(Q, K, V, perm=None, vsmooth: int = 1):
     if perm is not None:
         perm = np.ascontiguousarray(perm, dtype=np.int32)
         p = perm.ctypes.data_as(ctypes.c_void_p)
-    rc = lib().vco_quantize(Q, K, V, B, H, N, d, sb, sn, sh, p, int(vsmooth),
-                            out["Q8"], out["sq"], out["K8"], out["sk"], out["V8T"], out["sv"],
-                            out["mu"].ctypes.data_as(ctypes.c_void_p))
+    r, rp = _rope_table(rope, N, d)
+    rc = lib().vco_quantize_ex(Q, K, V, B, H, N, d, sb, sn, sh, p, int(vsmooth), rp, int(hadamard),
+                               out["Q8"], out["sq"], out["K8"], out["sk"], out["V8T"], out["sv"],
+                               out["mu"].ctypes.data_as(ctypes.c_void_p))
     assert rc == 0
     return out
 

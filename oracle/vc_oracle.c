@@ -246,49 +246,113 @@ int vco_argsort_labels(const int32_t* labels, int BH, int N, int k, int32_t* per
 /*  s_v [B,H,d]; mu [B,H,nblk,d] (bf16 bits).                           */
 /* ------------------------------------------------------------------ */
 
+/* ------------------------------------------------------------------ */
+/* Preprocessing of Q and K ahead of their quantizer: the rotary        */
+/* transform and the Hadamard rotation, two of the steps the pages'     */
+/* fused quantization kernel absorbs together with the block means,     */
+/* the gather and the quantizers ([R] 核心方法, the engineering          */
+/* sentence; [D] 3-1 "Fused CuTe kernel" row and 3-3 "Kernel fusion").  */
+/* The Hadamard rotation of the Q/K channels is the one FlashAttention-3 */
+/* applies before FP8 ([R] 研究动机).  The pages give neither formula;   */
+/* the readings taken:                                                  */
+/*  rotary   the channel pair (2i, 2i+1) of a token at position t is    */
+/*           rotated by an angle theta_{t,i} whose (cos, sin) the       */
+/*           caller tabulates in rope[t][i][0..1] (a complex64 table):  */
+/*             y0 = x0 c - x1 s,  y1 = x0 s + x1 c,                     */
+/*           each product rounded to fp32, then the difference / sum.   */
+/*           A K row is rotated at the position of the token it holds:  */
+/*           row t of K' = K[pi] uses position pi(t).                   */
+/*  Hadamard after the rotation, y <- H_d y with the Sylvester matrix   */
+/*           (H_d)_{ij} = (-1)^popcount(i & j), H_d H_d = d I, on every */
+/*           Q and K row; (H q).(H k) = d q.k, so the Q block scale     */
+/*           carries 1/d: s_q = (amax/448) * (1/d), exact because d is  */
+/*           a power of two.  Evaluated as the fast Walsh-Hadamard      */
+/*           transform: log2 d stages of butterflies (a, b) ->          */
+/*           (a + b, a - b), stride 1 first, every result rounded to    */
+/*           fp32, which fixes the rounding order.                      */
+/* ------------------------------------------------------------------ */
+
+static void preproc_row(const uint16_t* x, const float* rope_t, int hadamard, int d, float* y) {
+    for (int c = 0; c < d; ++c) y[c] = vco_bf16_to_f32(x[c]);
+    if (rope_t) {
+        for (int i = 0; i < d / 2; ++i) {
+            float cs = rope_t[2 * i], sn = rope_t[2 * i + 1];
+            float x0 = y[2 * i], x1 = y[2 * i + 1];
+            float a = x0 * cs, b = x1 * sn, e = x0 * sn, f = x1 * cs;
+            y[2 * i] = a - b;
+            y[2 * i + 1] = e + f;
+        }
+    }
+    if (hadamard) {
+        for (int st = 1; st < d; st <<= 1)
+            for (int i0 = 0; i0 < d; i0 += 2 * st)
+                for (int i = i0; i < i0 + st; ++i) {
+                    float a = y[i], b = y[i + st];
+                    y[i] = a + b;
+                    y[i + st] = a - b;
+                }
+    }
+}
+
+/* The preprocessed fp32 rows themselves, for the tests: rows X [n, d]   */
+/* (bf16 bits, contiguous), row r at position pos[r] (r if pos is NULL). */
+int vco_preproc_rows(const uint16_t* X, int64_t n, int d, const int32_t* pos,
+                     const float* rope, int hadamard, float* out) {
+    if (d < 1 || (rope && (d & 1)) || (hadamard && (d & (d - 1)))) return 1;
+    for (int64_t r = 0; r < n; ++r) {
+        int64_t t = pos ? pos[r] : r;
+        preproc_row(X + r * d, rope ? rope + t * d : NULL, hadamard, d, out + r * d);
+    }
+    return 0;
+}
+
 static void quant_rows_blockscale(const uint16_t* X, int64_t s_b, int64_t s_n, int64_t s_h,
                                   int b, int h, int N, int d, const int32_t* perm_bh,
+                                  const float* rope, int hadamard, float s_mul,
                                   uint8_t* X8, float* sx) {
     int nblk = (N + VCO_BLOCK - 1) / VCO_BLOCK;
+    float* Y = (float*)malloc(sizeof(float) * (size_t)VCO_BLOCK * d);
     for (int j = 0; j < nblk; ++j) {
         int t0 = j * VCO_BLOCK;
+        int cnt = (N - t0 < VCO_BLOCK) ? (N - t0) : VCO_BLOCK;
         float amax = 0.0f;
-        for (int t = t0; t < t0 + VCO_BLOCK && t < N; ++t) {
-            int src = perm_bh ? perm_bh[t] : t;
-            const uint16_t* x = tok(X, s_b, s_n, s_h, b, h, src);
+        for (int r = 0; r < cnt; ++r) {
+            int src = perm_bh ? perm_bh[t0 + r] : t0 + r;
+            preproc_row(tok(X, s_b, s_n, s_h, b, h, src), rope ? rope + (int64_t)src * d : NULL,
+                        hadamard, d, Y + (int64_t)r * d);
             for (int c = 0; c < d; ++c) {
-                float a = fabsf(vco_bf16_to_f32(x[c]));
+                float a = fabsf(Y[(int64_t)r * d + c]);
                 if (a > amax) amax = a;
             }
         }
         float s = amax / 448.0f;
         float inv = (amax > 0.0f) ? 448.0f / amax : 0.0f;
-        sx[j] = s;
-        for (int t = t0; t < t0 + VCO_BLOCK; ++t) {
-            uint8_t* out = X8 + (int64_t)t * d;
-            if (t >= N) { memset(out, 0, (size_t)d); continue; }
-            int src = perm_bh ? perm_bh[t] : t;
-            const uint16_t* x = tok(X, s_b, s_n, s_h, b, h, src);
-            for (int c = 0; c < d; ++c) out[c] = vco_e4m3_encode(vco_bf16_to_f32(x[c]) * inv);
+        sx[j] = s * s_mul;
+        for (int r = 0; r < VCO_BLOCK; ++r) {
+            uint8_t* out = X8 + (int64_t)(t0 + r) * d;
+            if (r >= cnt) { memset(out, 0, (size_t)d); continue; }
+            for (int c = 0; c < d; ++c) out[c] = vco_e4m3_encode(Y[(int64_t)r * d + c] * inv);
         }
     }
+    free(Y);
 }
 
-int vco_quantize(const uint16_t* Q, const uint16_t* K, const uint16_t* V,
-                 int B, int H, int N, int d, int64_t s_b, int64_t s_n, int64_t s_h,
-                 const int32_t* perm, int vsmooth,
-                 uint8_t* Q8, float* sq, uint8_t* K8, float* sk,
-                 uint8_t* V8T, float* sv, uint16_t* mu) {
-    if (N < 1 || d < 1) return 1;
+int vco_quantize_ex(const uint16_t* Q, const uint16_t* K, const uint16_t* V,
+                    int B, int H, int N, int d, int64_t s_b, int64_t s_n, int64_t s_h,
+                    const int32_t* perm, int vsmooth, const float* rope, int hadamard,
+                    uint8_t* Q8, float* sq, uint8_t* K8, float* sk,
+                    uint8_t* V8T, float* sv, uint16_t* mu) {
+    if (N < 1 || d < 1 || (rope && (d & 1)) || (hadamard && (d & (d - 1)))) return 1;
+    float q_mul = hadamard ? 1.0f / (float)d : 1.0f;
     int nblk = (N + VCO_BLOCK - 1) / VCO_BLOCK;
     int64_t Npad = (int64_t)nblk * VCO_BLOCK;
     #pragma omp parallel for schedule(dynamic)
     for (int bh = 0; bh < B * H; ++bh) {
         int b = bh / H, h = bh % H;
         const int32_t* p = perm ? perm + (int64_t)bh * N : NULL;
-        quant_rows_blockscale(Q, s_b, s_n, s_h, b, h, N, d, NULL,
+        quant_rows_blockscale(Q, s_b, s_n, s_h, b, h, N, d, NULL, rope, hadamard, q_mul,
                               Q8 + (int64_t)bh * Npad * d, sq + (int64_t)bh * nblk);
-        quant_rows_blockscale(K, s_b, s_n, s_h, b, h, N, d, p,
+        quant_rows_blockscale(K, s_b, s_n, s_h, b, h, N, d, p, rope, hadamard, 1.0f,
                               K8 + (int64_t)bh * Npad * d, sk + (int64_t)bh * nblk);
         /* V': block means, residuals, per-channel scale */
         float* R = (float*)malloc(sizeof(float) * (size_t)N * d);
@@ -328,6 +392,16 @@ int vco_quantize(const uint16_t* Q, const uint16_t* K, const uint16_t* V,
         free(R);
     }
     return 0;
+}
+
+/* The quantizer without the rotary transform and the Hadamard rotation. */
+int vco_quantize(const uint16_t* Q, const uint16_t* K, const uint16_t* V,
+                 int B, int H, int N, int d, int64_t s_b, int64_t s_n, int64_t s_h,
+                 const int32_t* perm, int vsmooth,
+                 uint8_t* Q8, float* sq, uint8_t* K8, float* sk,
+                 uint8_t* V8T, float* sv, uint16_t* mu) {
+    return vco_quantize_ex(Q, K, V, B, H, N, d, s_b, s_n, s_h, perm, vsmooth, NULL, 0,
+                           Q8, sq, K8, sk, V8T, sv, mu);
 }
 
 /* ------------------------------------------------------------------ */

@@ -1,6 +1,7 @@
 """Benchmark of the VC-Attention hot path on GB300.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--mode step|schedule|sweep]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--mode step|schedule|sweep|preproc]
 
 Default (mode=step): the Wan2.2-shaped workload (B=1, H=40, N=75,600, d=128,
 k=256).  One step = one grouping denoising step of the whole path: warm-started
@@ -11,6 +12,11 @@ metric is FP8 attention TFLOPS, 4 B H N^2 d per step divided by the step time
 Inputs (2.3 GB) are larger than the 129 MB L2, so no flush is needed between
 steps.  Under torchrun every rank runs the full workload on its own GPU (weak
 scaling, no collective on the data path); the time is the max over ranks.
+
+--mode preproc times the quantizer with the rotary transform and the Hadamard
+rotation of Q/K fused in (vc_quantize_ex) against the same computation run as
+the unfused chain of kernels (vc_quantize_staged), on the Wan2.2 shape with a
+21 x 45 x 80 rotary grid, plus the plain quantizer for reference.
 
 --impl reference times the CPU oracle (the only other implementation of the
 method that exists) on a bounded sample of the same workload.
@@ -38,13 +44,15 @@ def parse():
     ap.add_argument("--steps", type=int, default=5)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--mode", default="step", choices=["step", "schedule", "sweep"])
+    ap.add_argument("--mode", default="step", choices=["step", "schedule", "sweep", "preproc"])
     ap.add_argument("--expcast", type=int, default=1)
     ap.add_argument("--vsmooth", type=int, default=1)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--heads", type=int, default=0,
                     help="profiling aid: run the workload with this many heads instead of its own")
+    ap.add_argument("--arm", default="all", choices=["all", "plain", "fused", "unfused"],
+                    help="profiling aid for --mode preproc: time only this arm")
     return ap.parse_args()
 
 
@@ -434,6 +442,63 @@ def run_sweep(args):
     print(json.dumps({"mode": "sweep", "metric": "attention kernel TFLOPS, H=24 d=128", "rows": rows}), flush=True)
 
 
+def run_preproc(args):
+    """Fused vs unfused preprocessing chain (rotary, gather, block means,
+    Hadamard, FP8 quantization of Q/K/V) on the Wan2.2 shape."""
+    import torch
+
+    from bit_fp8_attention_means_gb300 import inputs, vc
+    dev = torch.device("cuda", 0)
+    w = inputs.WORKLOADS["wan"]
+    H = args.heads or w.H
+    Q, K, V = inputs.make_qkv(w, dev, H=H)
+    perm = vc.vc_cluster(V, w.k, w.iters)[2]
+    rope = torch.from_numpy(inputs.rope_table(w.N, w.d, inputs.WAN_GRID)).to(dev)
+    s = vc.shape_of(Q)
+    out = vc.alloc_quantized(s, dev, 1)
+    ws = torch.empty(vc.quantize_workspace_bytes(s), dtype=torch.uint8, device=dev)
+    ws_staged = torch.empty(vc.quantize_staged_workspace_bytes(s), dtype=torch.uint8, device=dev)
+    arms = {
+        "plain": lambda: vc.vc_quantize(Q, K, V, perm, 1, out=out, workspace=ws),
+        "fused": lambda: vc.vc_quantize_ex(Q, K, V, perm, 1, rope=rope, hadamard=1, out=out, workspace=ws),
+        "unfused": lambda: vc.vc_quantize_staged(Q, K, V, perm, 1, rope=rope, hadamard=1, out=out,
+                                                 workspace=ws_staged),
+    }
+    if args.arm != "all":
+        arms = {args.arm: arms[args.arm]}
+    reps = max(3, args.steps)
+    res = {}
+    for name, fn in arms.items():
+        for _ in range(max(3, args.warmup)):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        res[name] = e0.elapsed_time(e1) / reps
+    if args.arm != "all":
+        print(json.dumps({"mode": "preproc", "arm": args.arm, "ms": res[args.arm], "heads": H}), flush=True)
+        return
+    elems = w.B * w.N * H * w.d
+    # algorithmic bytes: Q, K, V read once (bf16), codes written (E4M3), the
+    # rotary table read once; scales, means and pi are < 1 %
+    alg = 3 * 2 * elems + 3 * elems + rope.numel() * 4
+    peak = measured_peaks()
+    print(json.dumps({
+        "mode": "preproc",
+        "metric": "Q/K/V preprocessing chain ms (rotary + gather + block means + Hadamard + FP8 quantization)",
+        "fused_ms": res["fused"], "unfused_ms": res["unfused"], "plain_quantizer_ms": res["plain"],
+        "fused_speedup": res["unfused"] / res["fused"],
+        "fused_gbs": alg / (res["fused"] * 1e-3) / 1e9, "algorithmic_bytes": alg,
+        "hbm_peak_gbs": peak["hbm_gbs"], "peak_source": peak["source"],
+        "unfused_workspace_bytes": ws_staged.numel(), "reps": reps,
+        "config": {"workload": "wan2.2-shaped B=1 H=%d N=75600 d=128, rotary grid 21x45x80, k=256 pi" % H,
+                   "l2": "inputs 2.3 GB > L2, no flush"}}), flush=True)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
@@ -443,6 +508,8 @@ def main():
         run_ours(args)
     elif args.mode == "schedule":
         run_schedule(args)
+    elif args.mode == "preproc":
+        run_preproc(args)
     else:
         run_sweep(args)
 

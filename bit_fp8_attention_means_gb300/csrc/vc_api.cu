@@ -40,7 +40,7 @@ const char* vc_status_string(vc_status s) {
     return "VC_ERR_UNKNOWN";
 }
 
-int vc_version(void) { return 100; }
+int vc_version(void) { return 101; }
 
 size_t vc_cluster_workspace(vc_shape shape, int k) {
     if (check_shape(shape) != VC_OK || k < 1) return 0;
@@ -69,21 +69,64 @@ size_t vc_quantize_workspace(vc_shape shape) {
     return quantize_workspace(shape);
 }
 
+static vc_status quantize_common(const void* Q, const void* K, const void* V, const vc_shape& shape, int vsmooth,
+                                 const float* rope, int hadamard, const uint8_t* Q8, const float* sq,
+                                 const uint8_t* K8, const float* sk, const uint8_t* V8T, const float* sv,
+                                 const void* mu) {
+    vc_status st = check_shape(shape);
+    if (st != VC_OK) return st;
+    if ((vsmooth != 0 && vsmooth != 1) || (hadamard != 0 && hadamard != 1)) return VC_ERR_INVALID_ARG;
+    if (!Q || !K || !V || !Q8 || !sq || !K8 || !sk || !V8T || !sv || (vsmooth && !mu)) return VC_ERR_INVALID_ARG;
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(Q8) || !aligned16(K8) || !aligned16(V8T) ||
+        !aligned16(rope))
+        return VC_ERR_INVALID_ARG;
+    return VC_OK;
+}
+
+static bool workspace_ok(const void* ws, size_t bytes, size_t need) {
+    return ws && bytes >= need && (reinterpret_cast<uintptr_t>(ws) & 255u) == 0;
+}
+
 vc_status vc_quantize(const void* Q, const void* K, const void* V, vc_shape shape, const int32_t* perm, int vsmooth,
                       uint8_t* Q8, float* sq, uint8_t* K8, float* sk, uint8_t* V8T, float* sv, void* mu,
                       void* workspace, size_t workspace_bytes, vc_stream_t stream) {
-    vc_status st = check_shape(shape);
+    return vc_quantize_ex(Q, K, V, shape, perm, vsmooth, nullptr, 0, Q8, sq, K8, sk, V8T, sv, mu, workspace,
+                          workspace_bytes, stream);
+}
+
+vc_status vc_quantize_ex(const void* Q, const void* K, const void* V, vc_shape shape, const int32_t* perm,
+                         int vsmooth, const float* rope, int hadamard, uint8_t* Q8, float* sq, uint8_t* K8,
+                         float* sk, uint8_t* V8T, float* sv, void* mu, void* workspace, size_t workspace_bytes,
+                         vc_stream_t stream) {
+    vc_status st = quantize_common(Q, K, V, shape, vsmooth, rope, hadamard, Q8, sq, K8, sk, V8T, sv, mu);
     if (st != VC_OK) return st;
-    if (vsmooth != 0 && vsmooth != 1) return VC_ERR_INVALID_ARG;
-    if (!Q || !K || !V || !Q8 || !sq || !K8 || !sk || !V8T || !sv || (vsmooth && !mu)) return VC_ERR_INVALID_ARG;
-    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(Q8) || !aligned16(K8) || !aligned16(V8T))
-        return VC_ERR_INVALID_ARG;
-    if (!workspace || workspace_bytes < quantize_workspace(shape) ||
-        (reinterpret_cast<uintptr_t>(workspace) & 255u))
-        return VC_ERR_WORKSPACE;
+    if (!workspace_ok(workspace, workspace_bytes, quantize_workspace(shape))) return VC_ERR_WORKSPACE;
+    Preproc pp;
+    pp.rope = rope;
+    pp.hadamard = hadamard;
     return launch_quantize(static_cast<const uint16_t*>(Q), static_cast<const uint16_t*>(K),
-                           static_cast<const uint16_t*>(V), shape, perm, vsmooth, Q8, sq, K8, sk, V8T, sv,
+                           static_cast<const uint16_t*>(V), shape, perm, vsmooth, pp, Q8, sq, K8, sk, V8T, sv,
                            static_cast<uint16_t*>(mu), workspace, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t vc_quantize_staged_workspace(vc_shape shape) {
+    if (check_shape(shape) != VC_OK) return 0;
+    return quantize_staged_workspace(shape);
+}
+
+vc_status vc_quantize_staged(const void* Q, const void* K, const void* V, vc_shape shape, const int32_t* perm,
+                             int vsmooth, const float* rope, int hadamard, uint8_t* Q8, float* sq, uint8_t* K8,
+                             float* sk, uint8_t* V8T, float* sv, void* mu, void* workspace, size_t workspace_bytes,
+                             vc_stream_t stream) {
+    vc_status st = quantize_common(Q, K, V, shape, vsmooth, rope, hadamard, Q8, sq, K8, sk, V8T, sv, mu);
+    if (st != VC_OK) return st;
+    if (!workspace_ok(workspace, workspace_bytes, quantize_staged_workspace(shape))) return VC_ERR_WORKSPACE;
+    Preproc pp;
+    pp.rope = rope;
+    pp.hadamard = hadamard;
+    return launch_quantize_staged(static_cast<const uint16_t*>(Q), static_cast<const uint16_t*>(K),
+                                  static_cast<const uint16_t*>(V), shape, perm, vsmooth, pp, Q8, sq, K8, sk, V8T,
+                                  sv, static_cast<uint16_t*>(mu), workspace, reinterpret_cast<cudaStream_t>(stream));
 }
 
 static vc_status attn_common(const uint8_t* Q8, const float* sq, const uint8_t* K8, const float* sk,

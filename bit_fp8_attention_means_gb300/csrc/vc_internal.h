@@ -21,10 +21,19 @@ vc_status cuda_status(cudaError_t e);
 PFN_cuTensorMapEncodeTiled_v12000 encode_tiled_fn();
 
 // quantizer (vc_quantize.cu)
+struct Preproc {
+    const float* rope = nullptr;  // [N, d/2, 2] (cos, sin), or null: no rotary transform
+    int hadamard = 0;             // 1: Walsh-Hadamard transform of Q and K rows, 1/d on the Q scale
+};
 size_t quantize_workspace(const vc_shape& s);
+size_t quantize_staged_workspace(const vc_shape& s);
 vc_status launch_quantize(const uint16_t* Q, const uint16_t* K, const uint16_t* V, const vc_shape& s,
-                          const int32_t* perm, int vsmooth, uint8_t* Q8, float* sq, uint8_t* K8, float* sk,
-                          uint8_t* V8T, float* sv, uint16_t* mu, void* ws, cudaStream_t st);
+                          const int32_t* perm, int vsmooth, const Preproc& pp, uint8_t* Q8, float* sq, uint8_t* K8,
+                          float* sk, uint8_t* V8T, float* sv, uint16_t* mu, void* ws, cudaStream_t st);
+vc_status launch_quantize_staged(const uint16_t* Q, const uint16_t* K, const uint16_t* V, const vc_shape& s,
+                                 const int32_t* perm, int vsmooth, const Preproc& pp, uint8_t* Q8, float* sq,
+                                 uint8_t* K8, float* sk, uint8_t* V8T, float* sv, uint16_t* mu, void* ws,
+                                 cudaStream_t st);
 
 // grouping (vc_cluster.cu)
 size_t cluster_workspace(const vc_shape& s, int k);

@@ -68,11 +68,11 @@ def _gen(seed: int, device) -> torch.Generator:
     return g
 
 
-def _outlier_channels(w: Workload, h: int, g: torch.Generator, device) -> torch.Tensor:
+def _outlier_channels(w: Workload, d: int, h: int, g: torch.Generator, device) -> torch.Tensor:
     if w.outlier_mode == "drift":
-        base = torch.randperm(w.d, generator=g, device=device)[:4]
-        return (base + 3 * h) % w.d
-    return torch.randperm(w.d, generator=g, device=device)[:4]
+        base = torch.randperm(d, generator=g, device=device)[:4]
+        return (base + 3 * h) % d
+    return torch.randperm(d, generator=g, device=device)[:4]
 
 
 def make_qkv(w: Workload, device="cpu", B=None, H=None, N=None, d=None, seed=None):
@@ -103,7 +103,7 @@ def make_qkv(w: Workload, device="cpu", B=None, H=None, N=None, d=None, seed=Non
             member = torch.randint(0, w.centers, (N,), generator=g, device=dev)
             v = centers[member] + (0.1 ** 0.5) * torch.randn((N, d), generator=g, device=dev)
             rows = torch.rand((N,), generator=g, device=dev) < 0.01
-            ch = _outlier_channels(w, h, g, dev)
+            ch = _outlier_channels(w, d, h, g, dev)
             scale = torch.ones((N, d), device=dev)
             scale[rows.nonzero().flatten()[:, None], ch[None, :]] = 20.0
             v = v * scale

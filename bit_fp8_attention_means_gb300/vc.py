@@ -53,6 +53,13 @@ def lib():
         L.vc_quantize.restype = ctypes.c_int
         L.vc_quantize.argtypes = [_vp, _vp, _vp, VcShape, _vp, ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                   _vp, ctypes.c_size_t, _vp]
+        L.vc_quantize_ex.restype = ctypes.c_int
+        L.vc_quantize_ex.argtypes = [_vp, _vp, _vp, VcShape, _vp, ctypes.c_int, _vp, ctypes.c_int, _vp, _vp, _vp,
+                                     _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
+        L.vc_quantize_staged_workspace.restype = ctypes.c_size_t
+        L.vc_quantize_staged_workspace.argtypes = [VcShape]
+        L.vc_quantize_staged.restype = ctypes.c_int
+        L.vc_quantize_staged.argtypes = L.vc_quantize_ex.argtypes
         L.vc_attn_fwd.restype = ctypes.c_int
         L.vc_attn_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, VcShape, ctypes.c_float, ctypes.c_int,
                                   ctypes.c_int, _vp, _vp, _vp]
@@ -145,25 +152,73 @@ def alloc_quantized(shape: VcShape, device, vsmooth=1):
         mu=_empty((B, H, nb, d), torch.int16, device) if vsmooth else None)
 
 
-def vc_quantize(Q, K, V, perm=None, vsmooth=1, out=None, workspace=None, stream=None):
-    """Fused quantizer. Returns a dict with Q8, sq, K8, sk, V8T, sv, mu (mu is bf16 bits as int16)."""
+def _check_qkv(Q, K, V):
     s = shape_of(Q)
     if shape_of(K).N != s.N or shape_of(V).N != s.N:
         raise ValueError("Q, K, V shapes differ")
     if (K.stride(), V.stride()) != (Q.stride(), Q.stride()):
         raise ValueError("Q, K, V must share strides")
+    return s
+
+
+def _check_rope(rope, s: VcShape):
+    if rope is None:
+        return
+    if rope.dtype != torch.float32 or tuple(rope.shape) != (s.N, s.d // 2, 2) or not rope.is_contiguous():
+        raise ValueError("rope must be a contiguous fp32 [N, d/2, 2] (cos, sin) table")
+
+
+def _quantize_call(fn, name, Q, K, V, perm, vsmooth, rope, hadamard, out, workspace, need, stream):
+    s = _check_qkv(Q, K, V)
+    _check_rope(rope, s)
     dev = Q.device
     if out is None:
         out = alloc_quantized(s, dev, vsmooth)
-    need = lib().vc_quantize_workspace(s)
     if workspace is None:
-        workspace = _workspace(need, dev)
-    rc = lib().vc_quantize(_ptr(Q), _ptr(K), _ptr(V), s, _ptr(perm), int(vsmooth), _ptr(out["Q8"]),
-                           _ptr(out["sq"]), _ptr(out["K8"]), _ptr(out["sk"]), _ptr(out["V8T"]), _ptr(out["sv"]),
-                           _ptr(out["mu"]) if vsmooth else None, _ptr(workspace), workspace.numel(),
-                           _stream(stream))
+        workspace = _workspace(need(s), dev)
+    args = [_ptr(Q), _ptr(K), _ptr(V), s, _ptr(perm), int(vsmooth), _ptr(rope), int(hadamard),
+             _ptr(out["Q8"]), _ptr(out["sq"]), _ptr(out["K8"]), _ptr(out["sk"]), _ptr(out["V8T"]), _ptr(out["sv"]),
+             _ptr(out["mu"]) if vsmooth else None, _ptr(workspace), workspace.numel(), _stream(stream)]
+    _check(fn(*args), name)
+    return out
+
+
+def vc_quantize(Q, K, V, perm=None, vsmooth=1, out=None, workspace=None, stream=None):
+    """Fused quantizer. Returns a dict with Q8, sq, K8, sk, V8T, sv, mu (mu is bf16 bits as int16)."""
+    L = lib()
+    s = _check_qkv(Q, K, V)
+    dev = Q.device
+    if out is None:
+        out = alloc_quantized(s, dev, vsmooth)
+    if workspace is None:
+        workspace = _workspace(L.vc_quantize_workspace(s), dev)
+    rc = L.vc_quantize(_ptr(Q), _ptr(K), _ptr(V), s, _ptr(perm), int(vsmooth), _ptr(out["Q8"]),
+                       _ptr(out["sq"]), _ptr(out["K8"]), _ptr(out["sk"]), _ptr(out["V8T"]), _ptr(out["sv"]),
+                       _ptr(out["mu"]) if vsmooth else None, _ptr(workspace), workspace.numel(),
+                       _stream(stream))
     _check(rc, "vc_quantize")
     return out
+
+
+def vc_quantize_ex(Q, K, V, perm=None, vsmooth=1, rope=None, hadamard=0, out=None, workspace=None, stream=None):
+    """vc_quantize with the rotary transform (``rope``: fp32 [N, d/2, 2] (cos, sin)
+    table on the device) and/or the Hadamard rotation of Q and K fused in."""
+    L = lib()
+    return _quantize_call(L.vc_quantize_ex, "vc_quantize_ex", Q, K, V, perm, vsmooth, rope, hadamard, out,
+                          workspace, L.vc_quantize_workspace, stream)
+
+
+def vc_quantize_staged(Q, K, V, perm=None, vsmooth=1, rope=None, hadamard=0, out=None, workspace=None,
+                       stream=None):
+    """The same computation as vc_quantize_ex as the unfused chain of kernels
+    (intermediates in device memory); bit-identical outputs."""
+    L = lib()
+    return _quantize_call(L.vc_quantize_staged, "vc_quantize_staged", Q, K, V, perm, vsmooth, rope, hadamard, out,
+                          workspace, L.vc_quantize_staged_workspace, stream)
+
+
+def quantize_staged_workspace_bytes(shape: VcShape) -> int:
+    return lib().vc_quantize_staged_workspace(shape)
 
 
 def vc_attn_fwd(qz, shape: VcShape, softmax_scale=0.0, expcast=1, vsmooth=1, O=None, dev_status=None,

@@ -142,6 +142,66 @@ vc_status vc_quantize(const void* Q, const void* K, const void* V, vc_shape shap
                       void* workspace, size_t workspace_bytes, vc_stream_t stream);
 
 /*
+ * vc_quantize with the rotary transform and the Hadamard rotation of Q and K
+ * fused in: the rest of the preprocessing chain that the paper's fused
+ * quantization kernel absorbs together with the block means, the gather and
+ * the quantizers (paper summary 核心方法; dimensionstp.github.io 3-1 "Fused
+ * CuTe kernel" and 3-3 "Kernel fusion"; the Q/K Hadamard rotation is the one
+ * FlashAttention-3 applies before FP8, paper summary 研究动机).  Neither
+ * formula is printed in the paper's pages; this library computes, per Q row
+ * and K' row, in fp32 and in this order:
+ *
+ *   rope      fp32 [N, d/2, 2], 16-byte aligned, or NULL (no rotation): the
+ *             (cos, sin) of the rotary angle of every token position and
+ *             channel pair -- the memory layout of a complex64 [N, d/2]
+ *             table, shared by all batches and heads.  Channels (2i, 2i+1)
+ *             of a row holding token n become
+ *               y0 = fl(fl(x0 cos) - fl(x1 sin)),  y1 = fl(fl(x0 sin) + fl(x1 cos))
+ *             with (cos, sin) = rope[n][i]; row t of K' = K[perm] holds token
+ *             perm[t] and is rotated at that position (as if K were rotated
+ *             before the gather).
+ *   hadamard  1: then y <- H_d y with the Sylvester Hadamard matrix
+ *             (H_d)_ij = (-1)^popcount(i & j) (entries +-1, H_d H_d = d I),
+ *             evaluated as log2(d) butterfly stages (a, b) -> (a + b, a - b),
+ *             stride 1 first, each result rounded to fp32.  (H q).(H k) =
+ *             d q.k, so sq carries the 1/d: sq = fl(amax/448) * (1/d), exact
+ *             for d a power of two, and vc_attn_fwd needs no change.
+ *             0: no rotation.
+ *
+ * The transformed rows are then quantized exactly as in vc_quantize (block
+ * amax, codes E4M3_RNE_sat(y * 448/amax)); V is not transformed.  With
+ * rope = NULL and hadamard = 0 the call is vc_quantize, bit for bit.  Same
+ * workspace as vc_quantize (vc_quantize_workspace).
+ * Errors: as vc_quantize, plus VC_ERR_INVALID_ARG for hadamard not in {0,1}
+ * or a misaligned `rope`.
+ */
+vc_status vc_quantize_ex(const void* Q, const void* K, const void* V, vc_shape shape,
+                         const int32_t* perm, int vsmooth, const float* rope, int hadamard,
+                         uint8_t* Q8, float* sq, uint8_t* K8, float* sk,
+                         uint8_t* V8T, float* sv, void* mu,
+                         void* workspace, size_t workspace_bytes, vc_stream_t stream);
+
+/*
+ * The computation of vc_quantize_ex run as the unfused chain: one kernel per
+ * step, each step's result written to device memory and read back by the
+ * next -- rotary transform (Q and K to fp32 [B,N,H,d]), gather of K' (fp32)
+ * and V' (bf16) into [B,H,N,d], Hadamard rotation in place, V block means
+ * and residual maxima, Q/K block quantization, V residual codes.  Every step
+ * rounds as the fused kernels do, so all outputs are bit-identical to
+ * vc_quantize_ex; it is there to measure what the fusion saves (the paper
+ * reports its fused chain against the unfused one, paper summary 核心方法).
+ * The workspace holds the intermediates: vc_quantize_staged_workspace(shape)
+ * = the vc_quantize workspace + 14 B*N*H*d bytes (+ alignment), 256-byte
+ * aligned.  Same arguments, errors and results as vc_quantize_ex.
+ */
+size_t vc_quantize_staged_workspace(vc_shape shape);
+vc_status vc_quantize_staged(const void* Q, const void* K, const void* V, vc_shape shape,
+                             const int32_t* perm, int vsmooth, const float* rope, int hadamard,
+                             uint8_t* Q8, float* sq, uint8_t* K8, float* sk,
+                             uint8_t* V8T, float* sv, void* mu,
+                             void* workspace, size_t workspace_bytes, vc_stream_t stream);
+
+/*
  * vc_quantize without a workspace argument, for callers that cannot allocate
  * device memory: a host that embeds this library inside a framework whose
  * memory pool owns all device memory, or code running where an allocation

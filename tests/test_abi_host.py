@@ -91,3 +91,20 @@ def test_quantize_and_cluster_argument_errors(L):
     small = _shape(N=4)
     assert L.vc_cluster(FAKE, small, 8, 1, 0, FAKE, FAKE, FAKE, FAKE, 1 << 20, None, None) == 1
     assert L.vc_debug_wait_timeout(None, 10, None) == 1
+
+
+def test_quantize_ex_and_staged_argument_errors(L):
+    s = _shape()
+    f = [FAKE] * 3
+    outs = [FAKE] * 7
+    ws_need = L.vc_quantize_workspace(s)
+    staged_need = L.vc_quantize_staged_workspace(s)
+    elems = 1 * 1000 * 2 * 128
+    assert staged_need >= ws_need + 14 * elems
+    unaligned = ctypes.c_void_p(0x10008)
+    for fn, need in ((L.vc_quantize_ex, ws_need), (L.vc_quantize_staged, staged_need)):
+        assert fn(*f, s, None, 1, None, 2, *outs, FAKE, need, None) == 1        # hadamard flag
+        assert fn(*f, s, None, 1, unaligned, 1, *outs, FAKE, need, None) == 1   # rope alignment
+        assert fn(*f, s, None, 1, FAKE, 1, *outs, FAKE, need - 1, None) == 3
+        assert fn(*f, _shape(d=96), None, 1, FAKE, 1, *outs, FAKE, need, None) == 2
+    assert L.vc_quantize_staged_workspace(_shape(d=96)) == 0

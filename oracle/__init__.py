@@ -56,6 +56,8 @@ def lib():
                                  _int, _int, _int, _f32p, _i32p]
         L.vco_argsort_labels.restype = _int
         L.vco_argsort_labels.argtypes = [_i32p, _int, _int, _int, _i32p]
+        L.vco_block_fill.restype = _int
+        L.vco_block_fill.argtypes = [_i32p, _f32p, _int, _int, _int, _int, _i32p]
         L.vco_quantize.restype = _int
         L.vco_quantize.argtypes = [_u16p, _u16p, _u16p, _int, _int, _int, _int, _i64, _i64, _i64,
                                    ctypes.c_void_p, _int, _u8p, _f32p, _u8p, _f32p, _u8p, _f32p,
@@ -183,6 +185,19 @@ def preproc_rows(X, pos=None, rope=None, hadamard: int = 0) -> np.ndarray:
     rp = r.ctypes.data_as(ctypes.c_void_p) if r is not None else None
     assert lib().vco_preproc_rows(X, n, d, pp, rp, int(hadamard), out) == 0
     return out
+
+
+def block_fill(labels, centroids) -> np.ndarray:
+    """Block-fill permutation [B,H,N] from labels [B,H,N] and centroids [B,H,k,d]:
+    whole 128-token blocks of each cluster in label order, then the clusters'
+    leftovers along a greedy nearest-centroid chain."""
+    z = np.ascontiguousarray(labels, dtype=np.int32)
+    C = np.ascontiguousarray(centroids, dtype=np.float32)
+    B, H, N = z.shape
+    k, d = C.shape[2], C.shape[3]
+    perm = np.zeros_like(z)
+    assert lib().vco_block_fill(z, C, B * H, N, k, d, perm) == 0
+    return perm
 
 
 def quantize(Q, K, V, perm=None, vsmooth: int = 1, rope=None, hadamard: int = 0):

@@ -227,6 +227,76 @@ int vco_argsort_labels(const int32_t* labels, int BH, int N, int k, int32_t* per
 }
 
 /* ------------------------------------------------------------------ */
+/* Block fill: a permutation that keeps whole 128-token blocks inside    */
+/* one cluster and places the partial blocks of similar clusters next   */
+/* to each other.  The pages' own analysis (paper summary, 独立分析的弱点 */
+/* weakness one) notes that balanced k-means lowers the V error but      */
+/* costs 2.8x the grouping time, and proposes cheap balancing instead:   */
+/* a greedy backfill or local exchanges at block boundaries.  Reading    */
+/* taken (any order of K/V is exact, P'V' = PV):                         */
+/*   n_c members of cluster c (token order), f_c = n_c - n_c mod 128     */
+/*   whole-block members, l_c = n_c mod 128 leftovers.                   */
+/*   1. all whole blocks, clusters in label order;                        */
+/*   2. the leftovers, clusters in the order of a greedy chain over the  */
+/*      clusters with l_c > 0: start at the lowest such label, then      */
+/*      repeatedly the unvisited one whose centroid is nearest to the    */
+/*      last (squared distance summed over the channels in order, each   */
+/*      difference, square and sum rounded to fp32; ties to the lower   */
+/*      label).                                                          */
+/* With every n_c a multiple of 128 this is the stable argsort.          */
+/* ------------------------------------------------------------------ */
+
+int vco_block_fill(const int32_t* labels, const float* cent, int BH, int N, int k, int d,
+                   int32_t* perm) {
+    if (k < 1 || N < 1 || d < 1) return 1;
+    #pragma omp parallel for schedule(dynamic)
+    for (int bh = 0; bh < BH; ++bh) {
+        const int32_t* z = labels + (int64_t)bh * N;
+        const float* C = cent + (int64_t)bh * k * d;
+        int32_t* p = perm + (int64_t)bh * N;
+        int* n = (int*)calloc((size_t)k, sizeof(int));
+        int* chain = (int*)malloc(sizeof(int) * (size_t)k);
+        char* used = (char*)calloc((size_t)k, 1);
+        for (int t = 0; t < N; ++t) n[z[t]] += 1;
+        int pos = 0;
+        /* 1. whole blocks in label order */
+        for (int c = 0; c < k; ++c) {
+            int f = n[c] - n[c] % VCO_BLOCK, seen = 0;
+            for (int t = 0; t < N && seen < f; ++t)
+                if (z[t] == c) { p[pos++] = t; ++seen; }
+        }
+        /* 2. chain over the clusters with leftovers */
+        int nch = 0, last = -1;
+        for (int c = 0; c < k; ++c)
+            if (n[c] % VCO_BLOCK) { last = c; break; }
+        while (last >= 0) {
+            chain[nch++] = last;
+            used[last] = 1;
+            int best = -1;
+            float bestd = 0.0f;
+            for (int c = 0; c < k; ++c) {
+                if (used[c] || n[c] % VCO_BLOCK == 0) continue;
+                float sum = 0.0f;
+                for (int e = 0; e < d; ++e) {
+                    float df = C[(int64_t)c * d + e] - C[(int64_t)last * d + e];
+                    float sq = df * df;
+                    sum = sum + sq;
+                }
+                if (best < 0 || sum < bestd) { best = c; bestd = sum; }
+            }
+            last = best;
+        }
+        for (int i = 0; i < nch; ++i) {
+            int c = chain[i], f = n[c] - n[c] % VCO_BLOCK, seen = 0;
+            for (int t = 0; t < N; ++t)
+                if (z[t] == c) { if (seen >= f) p[pos++] = t; ++seen; }
+        }
+        free(n); free(chain); free(used);
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
 /* Step 2, block quantization.                                          */
 /*  Q and K' = K[pi]: one fp32 scale per 128-token block ([R] 前置知识  */
 /*  "低比特量化与离群值": every hardware block shares one scale s_X):   */

@@ -18,6 +18,11 @@ rotation of Q/K fused in (vc_quantize_ex) against the same computation run as
 the unfused chain of kernels (vc_quantize_staged), on the Wan2.2 shape with a
 21 x 45 x 80 rotary grid, plus the plain quantizer for reference.
 
+--mode fill compares the plain permutation (stable argsort of the k-means
+labels) with the block-fill permutation (vc_cluster_ex): grouping time, the
+relative error of the dequantized V', and the attention output against an
+fp64 reference on sampled query rows.
+
 --impl reference times the CPU oracle (the only other implementation of the
 method that exists) on a bounded sample of the same workload.
 """
@@ -44,7 +49,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=5)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--mode", default="step", choices=["step", "schedule", "sweep", "preproc"])
+    ap.add_argument("--mode", default="step", choices=["step", "schedule", "sweep", "preproc", "fill"])
     ap.add_argument("--expcast", type=int, default=1)
     ap.add_argument("--vsmooth", type=int, default=1)
     ap.add_argument("--no-e2e", action="store_true")
@@ -499,6 +504,67 @@ def run_preproc(args):
                    "l2": "inputs 2.3 GB > L2, no flush"}}), flush=True)
 
 
+def run_fill(args):
+    """Plain vs block-fill permutation on the Wan2.2 shape: grouping cost, V'
+    reconstruction error, attention error against fp64 on sampled rows."""
+    import torch
+
+    from bit_fp8_attention_means_gb300 import inputs, vc
+    dev = torch.device("cuda", 0)
+    w = inputs.WORKLOADS["wan"]
+    H = args.heads or w.H
+    Q, K, V = inputs.make_qkv(w, dev, H=H)
+    cent0, _, _ = vc.vc_cluster(V, w.k, w.iters)
+    s = vc.shape_of(Q)
+    res = {}
+    g = torch.Generator(device="cpu").manual_seed(7)
+    rows = torch.randperm(w.N, generator=g)[:256].to(dev)
+    heads = list(range(0, H, max(1, H // 4)))[:4]
+    # fp64 reference rows, per sampled head
+    ref = {}
+    for h in heads:
+        q = Q[0, rows, h].double()
+        k = K[0, :, h].double()
+        v = V[0, :, h].double()
+        p = torch.softmax(q @ k.T / math.sqrt(w.d), dim=-1)
+        ref[h] = p @ v
+    for fill in (0, 1):
+        cent = cent0.clone()
+        fn = lambda: vc.vc_cluster(V, w.k, 1, warm_start=True, centroids=cent.copy_(cent0), block_fill=fill)
+        for _ in range(max(3, args.warmup)):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = max(3, args.steps)
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        _, _, perm = fn()
+        qz = vc.vc_quantize(Q, K, V, perm, 1)
+        O = vc.vc_attn_fwd(qz, s)
+        torch.cuda.synchronize()
+        # V' reconstruction: R codes * s_v + block mean, against V gathered by pi
+        Rq = qz["V8T"].view(torch.float8_e4m3fn).float() * qz["sv"][..., None]       # [B,H,d,Npad]
+        mu = qz["mu"].view(torch.bfloat16).float().repeat_interleave(128, dim=2)     # [B,H,Npad,d]
+        Vr = Rq.transpose(2, 3)[:, :, :w.N] + mu[:, :, :w.N]
+        Vp = torch.gather(V.permute(0, 2, 1, 3).float(), 2, perm.long()[..., None].expand(-1, -1, -1, w.d))
+        verr = float((Vr - Vp).norm() / Vp.norm())
+        mres = float((Vp - mu[:, :, :w.N]).norm() / Vp.norm())
+        oerr = [float((O[0, rows, h].double() - ref[h]).norm() / ref[h].norm()) for h in heads]
+        res[fill] = {"cluster_ms": ms, "v_rel_err": verr, "residual_energy": mres ** 2,
+                     "o_rel_err_vs_fp64": sum(oerr) / len(oerr)}
+    print(json.dumps({
+        "mode": "fill", "metric": "V' reconstruction error and attention error vs fp64, plain vs block-fill pi",
+        "plain": res[0], "block_fill": res[1],
+        "v_err_reduction": 1 - res[1]["v_rel_err"] / res[0]["v_rel_err"],
+        "fill_overhead_ms": res[1]["cluster_ms"] - res[0]["cluster_ms"],
+        "config": {"workload": "wan2.2-shaped B=1 H=%d N=75600 d=128 k=256, warm k-means step (1 iteration)" % H,
+                   "sampled_rows": 256, "sampled_heads": heads}}), flush=True)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
@@ -510,6 +576,8 @@ def main():
         run_schedule(args)
     elif args.mode == "preproc":
         run_preproc(args)
+    elif args.mode == "fill":
+        run_fill(args)
     else:
         run_sweep(args)
 

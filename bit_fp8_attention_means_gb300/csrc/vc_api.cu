@@ -50,18 +50,26 @@ size_t vc_cluster_workspace(vc_shape shape, int k) {
 vc_status vc_cluster(const void* V, vc_shape shape, int k, int iters, int warm_start, float* centroids,
                      int32_t* labels, int32_t* perm, void* workspace, size_t workspace_bytes, int32_t* dev_status,
                      vc_stream_t stream) {
+    return vc_cluster_ex(V, shape, k, iters, warm_start, 0, centroids, labels, perm, workspace, workspace_bytes,
+                         dev_status, stream);
+}
+
+vc_status vc_cluster_ex(const void* V, vc_shape shape, int k, int iters, int warm_start, int block_fill,
+                        float* centroids, int32_t* labels, int32_t* perm, void* workspace, size_t workspace_bytes,
+                        int32_t* dev_status, vc_stream_t stream) {
     vc_status st = check_shape(shape);
     if (st != VC_OK) return st;
     if (!V || !centroids || !labels || !perm) return VC_ERR_INVALID_ARG;
     if (!aligned16(V) || !aligned16(centroids)) return VC_ERR_INVALID_ARG;
-    if (iters < 1 || (warm_start != 0 && warm_start != 1)) return VC_ERR_INVALID_ARG;
+    if (iters < 1 || (warm_start != 0 && warm_start != 1) || (block_fill != 0 && block_fill != 1))
+        return VC_ERR_INVALID_ARG;
     if (k < 1 || k > 1024) return VC_ERR_UNSUPPORTED;
     if (k > shape.N) return VC_ERR_INVALID_ARG;
     if (!workspace || workspace_bytes < cluster_workspace(shape, k) ||
         (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return VC_ERR_WORKSPACE;
-    return launch_cluster(static_cast<const uint16_t*>(V), shape, k, iters, warm_start, centroids, labels, perm,
-                          workspace, dev_status, reinterpret_cast<cudaStream_t>(stream));
+    return launch_cluster(static_cast<const uint16_t*>(V), shape, k, iters, warm_start, block_fill, centroids, labels,
+                          perm, workspace, dev_status, reinterpret_cast<cudaStream_t>(stream));
 }
 
 size_t vc_quantize_workspace(vc_shape shape) {

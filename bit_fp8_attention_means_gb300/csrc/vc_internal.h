@@ -37,7 +37,7 @@ vc_status launch_quantize_staged(const uint16_t* Q, const uint16_t* K, const uin
 
 // grouping (vc_cluster.cu)
 size_t cluster_workspace(const vc_shape& s, int k);
-vc_status launch_cluster(const uint16_t* V, const vc_shape& s, int k, int iters, int warm, float* cent,
+vc_status launch_cluster(const uint16_t* V, const vc_shape& s, int k, int iters, int warm, int fill, float* cent,
                          int32_t* labels, int32_t* perm, void* ws, int32_t* dev_status, cudaStream_t st);
 
 // attention (vc_attn.cu)

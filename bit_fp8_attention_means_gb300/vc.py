@@ -48,6 +48,9 @@ def lib():
         L.vc_cluster.restype = ctypes.c_int
         L.vc_cluster.argtypes = [_vp, VcShape, ctypes.c_int, ctypes.c_int, ctypes.c_int, _vp, _vp, _vp, _vp,
                                  ctypes.c_size_t, _vp, _vp]
+        L.vc_cluster_ex.restype = ctypes.c_int
+        L.vc_cluster_ex.argtypes = [_vp, VcShape, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, _vp, _vp,
+                                    _vp, _vp, ctypes.c_size_t, _vp, _vp]
         L.vc_quantize_workspace.restype = ctypes.c_size_t
         L.vc_quantize_workspace.argtypes = [VcShape]
         L.vc_quantize.restype = ctypes.c_int
@@ -120,8 +123,11 @@ def _workspace(nbytes, device):
 
 
 def vc_cluster(V, k, iters, warm_start=False, centroids=None, labels=None, perm=None, workspace=None,
-               dev_status=None, stream=None):
-    """Grouping step. Returns (centroids fp32 [B,H,k,d], labels int32 [B,H,N], perm int32 [B,H,N])."""
+               dev_status=None, stream=None, block_fill=0):
+    """Grouping step. Returns (centroids fp32 [B,H,k,d], labels int32 [B,H,N], perm int32 [B,H,N]).
+
+    block_fill=1 calls vc_cluster_ex: perm keeps whole 128-token blocks per
+    cluster and chains the clusters' leftovers by centroid distance."""
     s = shape_of(V)
     dev = V.device
     if centroids is None:
@@ -135,6 +141,12 @@ def vc_cluster(V, k, iters, warm_start=False, centroids=None, labels=None, perm=
     need = lib().vc_cluster_workspace(s, k)
     if workspace is None:
         workspace = _workspace(need, dev)
+    if block_fill:
+        rc = lib().vc_cluster_ex(_ptr(V), s, k, iters, int(bool(warm_start)), int(block_fill), _ptr(centroids),
+                                 _ptr(labels), _ptr(perm), _ptr(workspace), workspace.numel(), _ptr(dev_status),
+                                 _stream(stream))
+        _check(rc, "vc_cluster_ex")
+        return centroids, labels, perm
     rc = lib().vc_cluster(_ptr(V), s, k, iters, int(bool(warm_start)), _ptr(centroids), _ptr(labels), _ptr(perm),
                           _ptr(workspace), workspace.numel(), _ptr(dev_status), _stream(stream))
     _check(rc, "vc_cluster")

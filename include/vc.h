@@ -113,6 +113,31 @@ vc_status vc_cluster(const void* V, vc_shape shape, int k, int iters, int warm_s
                      int32_t* dev_status, vc_stream_t stream);
 
 /*
+ * vc_cluster with an optional block-fill permutation.  The paper summary's own
+ * analysis (独立分析的弱点, weakness one) observes that balanced k-means lowers
+ * the V error but costs 2.8x the grouping time, and proposes cheap balancing
+ * of the block fill instead (greedy backfill, or exchanges at block
+ * boundaries).  With block_fill = 1, perm is instead:
+ *   1. every cluster's whole 128-token blocks -- its first n_c - (n_c mod 128)
+ *      members in token order -- with the clusters in label order;
+ *   2. then the clusters' leftovers (their last n_c mod 128 members, token
+ *      order), the clusters ordered by a greedy chain: start at the lowest
+ *      label that has leftovers, then repeatedly the unvisited cluster with
+ *      leftovers whose centroid is nearest to the last one (squared distance
+ *      over the channels in order, each difference, square and sum rounded
+ *      to fp32; ties to the lower label), using the returned centroids.
+ * Any order of K and V leaves attention exact (P'V' = PV); this one puts
+ * similar tokens into the partial blocks, so their means remove more.  With
+ * every cluster size a multiple of 128 it equals the stable argsort.
+ * block_fill = 0 is vc_cluster.  Same workspace query and errors as
+ * vc_cluster, plus VC_ERR_INVALID_ARG for block_fill not in {0, 1}.
+ */
+vc_status vc_cluster_ex(const void* V, vc_shape shape, int k, int iters, int warm_start, int block_fill,
+                        float* centroids, int32_t* labels, int32_t* perm,
+                        void* workspace, size_t workspace_bytes,
+                        int32_t* dev_status, vc_stream_t stream);
+
+/*
  * Fused quantizer, paper summary 方法步骤详情 step 2 and 前置知识 "低比特量化与
  * 离群值"; dimensionstp.github.io 2-2 (mu_j = (1/B_v) V'_j^T 1, R_j = V'_j - 1 mu_j^T).
  *

@@ -91,6 +91,8 @@ def test_quantize_and_cluster_argument_errors(L):
     small = _shape(N=4)
     assert L.vc_cluster(FAKE, small, 8, 1, 0, FAKE, FAKE, FAKE, FAKE, 1 << 20, None, None) == 1
     assert L.vc_debug_wait_timeout(None, 10, None) == 1
+    assert L.vc_cluster_ex(FAKE, s, 8, 1, 0, 2, FAKE, FAKE, FAKE, FAKE, cw, None, None) == 1   # block_fill flag
+    assert L.vc_cluster_ex(FAKE, s, 8, 1, 0, 1, FAKE, FAKE, FAKE, FAKE, cw - 1, None, None) == 3
 
 
 def test_quantize_ex_and_staged_argument_errors(L):

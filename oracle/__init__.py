@@ -72,6 +72,10 @@ def lib():
         L.vco_attn.argtypes = [_u8p, _f32p, _u8p, _f32p, _u8p, _f32p, ctypes.c_void_p,
                                _int, _int, _int, _int, ctypes.c_float, _int, _int,
                                _i32p, _int, ctypes.c_void_p, _f64p, ctypes.c_void_p]
+        L.vco_attn_ex.restype = _int
+        L.vco_attn_ex.argtypes = [_u8p, _f32p, _u8p, _f32p, _u8p, _f32p, ctypes.c_void_p,
+                                  _int, _int, _int, _int, ctypes.c_float, _int, ctypes.c_float, _int,
+                                  _i32p, _int, ctypes.c_void_p, _f64p, ctypes.c_void_p]
         L.vco_attn_ref.restype = _int
         L.vco_attn_ref.argtypes = [_u16p, _u16p, _u16p, _int, _int, _int, _int, _i64, _i64, _i64,
                                    ctypes.c_double, _i32p, _int, _f64p]
@@ -228,10 +232,14 @@ def quantize(Q, K, V, perm=None, vsmooth: int = 1, rope=None, hadamard: int = 0)
 
 
 def attn(qz: dict, N: int, softmax_scale: float = 0.0, expcast: int = 1, vsmooth: int = 1,
-         rows=None, acc_in=None, want_codes: bool = False):
+         rows=None, acc_in=None, want_codes: bool = False, margin: float = 0.0):
     """Quantized-path attention for the query rows ``rows`` of every (b,h).
 
-    Returns O fp64 [B,H,nrows,d] (and codes uint8 [B,H,nrows,Npad] if asked).
+    expcast: 0 exp-then-cast, 1 ExpCast, 2 hybrid (exp-then-cast on the key
+    tiles that are high-weight for a 32-row group: some row's tile maximum
+    within ``margin`` (log2 units) of its running maximum; ``rows`` must then
+    hold whole groups).  Returns O fp64 [B,H,nrows,d] (and codes uint8
+    [B,H,nrows,Npad] if asked).
     """
     B, H, Npad, d = qz["Q8"].shape
     if rows is None:
@@ -246,13 +254,13 @@ def attn(qz: dict, N: int, softmax_scale: float = 0.0, expcast: int = 1, vsmooth
         assert acc_in.shape == (B, H, nr, Npad)
         acc_p = acc_in.ctypes.data_as(ctypes.c_void_p)
     mu = np.ascontiguousarray(qz["mu"], dtype=np.uint16)
-    rc = lib().vco_attn(np.ascontiguousarray(qz["Q8"]), np.ascontiguousarray(qz["sq"]),
-                        np.ascontiguousarray(qz["K8"]), np.ascontiguousarray(qz["sk"]),
-                        np.ascontiguousarray(qz["V8T"]), np.ascontiguousarray(qz["sv"]),
-                        mu.ctypes.data_as(ctypes.c_void_p),
-                        B, H, N, d, float(kscale_of(softmax_scale, d)), int(expcast), int(vsmooth),
-                        rows, nr, acc_p, O,
-                        P.ctypes.data_as(ctypes.c_void_p) if P is not None else None)
+    rc = lib().vco_attn_ex(np.ascontiguousarray(qz["Q8"]), np.ascontiguousarray(qz["sq"]),
+                           np.ascontiguousarray(qz["K8"]), np.ascontiguousarray(qz["sk"]),
+                           np.ascontiguousarray(qz["V8T"]), np.ascontiguousarray(qz["sv"]),
+                           mu.ctypes.data_as(ctypes.c_void_p),
+                           B, H, N, d, float(kscale_of(softmax_scale, d)), int(expcast), float(margin),
+                           int(vsmooth), rows, nr, acc_p, O,
+                           P.ctypes.data_as(ctypes.c_void_p) if P is not None else None)
     assert rc == 0
     return (O, P) if want_codes else O
 

@@ -495,17 +495,79 @@ int vco_quantize(const uint16_t* Q, const uint16_t* K, const uint16_t* V,
 /* fp32 scores); P_out, when given, receives the codes.                 */
 /* ------------------------------------------------------------------ */
 
-int vco_attn(const uint8_t* Q8, const float* sq, const uint8_t* K8, const float* sk,
-             const uint8_t* V8T, const float* sv, const uint16_t* mu,
-             int B, int H, int N, int d, float kscale, int expcast, int vsmooth,
-             const int32_t* rows, int nrows, const float* acc_in,
-             double* O /* [B,H,nrows,d] */, uint8_t* P_out /* [B,H,nrows,Npad] or NULL */) {
-    if (N < 1 || d < 1) return 1;
+/* Hybrid probability bytes (expcast = 2).  The pages' own analysis (paper    */
+/* summary, 独立分析的弱点, weakness two) notes that the fixed beta costs     */
+/* 0.7-2.1 dB and proposes keeping the exact exponent on high-weight tiles    */
+/* (a mixed-precision softmax).  Reading: query rows are taken in groups of   */
+/* 32 consecutive rows of a 128-row query tile (the rows >= N excluded); key  */
+/* tile j is high-weight for a group if, for some row of it,                  */
+/* fl(sigma*mx) - m' >= -margin (fp32, log2 units: the tile holds a           */
+/* probability >= 2^-margin of the row's running maximum).  Such a tile is    */
+/* written with exp-then-cast for every row of the group, any other tile with */
+/* the ExpCast byte.  Whole groups must be requested together.                */
+static int hybrid_flags(const uint8_t* Q8, const float* sq, const uint8_t* K8, const float* sk,
+                        int bh, int N, int d, int nblk, int64_t Npad, float kscale, float margin,
+                        const int32_t* rows, int nrows, const float* acc_in, const double* dec,
+                        uint8_t* flags /* [ngroups][nblk] */) {
+    int ngroups = (int)(Npad / 32);
+    int* present = (int*)calloc((size_t)ngroups, sizeof(int));
+    for (int ri = 0; ri < nrows; ++ri) present[rows[ri] / 32] += 1;
+    for (int g = 0; g < ngroups; ++g) {
+        int valid = N - g * 32;
+        valid = valid < 0 ? 0 : (valid > 32 ? 32 : valid);
+        if (present[g] && present[g] != valid) { free(present); return 1; }
+    }
+    free(present);
+    memset(flags, 0, (size_t)ngroups * nblk);
+    for (int ri = 0; ri < nrows; ++ri) {
+        int i = rows[ri], g = i / 32;
+        const uint8_t* q = Q8 + ((int64_t)bh * Npad + i) * d;
+        float sqi = sq[(int64_t)bh * nblk + i / VCO_BLOCK];
+        float m = -INFINITY;
+        for (int j = 0; j < nblk; ++j) {
+            int t0 = j * VCO_BLOCK;
+            int cnt = (N - t0 < VCO_BLOCK) ? (N - t0) : VCO_BLOCK;
+            float sigma = (sqi * sk[(int64_t)bh * nblk + j]) * kscale;
+            float mx = -INFINITY;
+            for (int kk = 0; kk < cnt; ++kk) {
+                float a;
+                if (acc_in) {
+                    a = acc_in[((int64_t)bh * nrows + ri) * Npad + t0 + kk];
+                } else {
+                    const uint8_t* kr = K8 + ((int64_t)bh * Npad + t0 + kk) * d;
+                    double sacc = 0.0;
+                    for (int c = 0; c < d; ++c) sacc += dec[q[c]] * dec[kr[c]];
+                    a = (float)sacc;
+                }
+                if (a > mx) mx = a;
+            }
+            float smx = sigma * mx;
+            float mnew = fmaxf(m, smx);
+            float diff = smx - mnew;
+            if (diff >= -margin) flags[(int64_t)g * nblk + j] = 1;
+            m = mnew;
+        }
+    }
+    return 0;
+}
+
+int vco_attn_ex(const uint8_t* Q8, const float* sq, const uint8_t* K8, const float* sk,
+                const uint8_t* V8T, const float* sv, const uint16_t* mu,
+                int B, int H, int N, int d, float kscale, int expcast, float margin, int vsmooth,
+                const int32_t* rows, int nrows, const float* acc_in,
+                double* O /* [B,H,nrows,d] */, uint8_t* P_out /* [B,H,nrows,Npad] or NULL */) {
+    if (N < 1 || d < 1 || expcast < 0 || expcast > 2) return 1;
     int nblk = (N + VCO_BLOCK - 1) / VCO_BLOCK;
     int64_t Npad = (int64_t)nblk * VCO_BLOCK;
     double dec[256];
     for (int i = 0; i < 256; ++i) dec[i] = vco_e4m3_decode((uint8_t)i);
+    uint8_t* flags = (expcast == 2) ? (uint8_t*)malloc((size_t)(Npad / 32) * nblk) : NULL;
     for (int bh = 0; bh < B * H; ++bh) {
+        if (flags && hybrid_flags(Q8, sq, K8, sk, bh, N, d, nblk, Npad, kscale, margin, rows, nrows, acc_in,
+                                  dec, flags)) {
+            free(flags);
+            return 1;
+        }
         /* decoded residual values in [token][channel] order */
         double* Vd = (double*)malloc(sizeof(double) * (size_t)Npad * d);
         for (int c = 0; c < d; ++c)
@@ -542,7 +604,7 @@ int vco_attn(const uint8_t* Q8, const float* sq, const uint8_t* K8, const float*
                 float mnew = fmaxf(m, sigma * mx);
                 double alpha = (m == -INFINITY) ? 0.0 : exp2((double)m - (double)mnew);
                 double r = 0.0;
-                if (expcast) {
+                if (expcast == 1 || (expcast == 2 && !flags[(int64_t)(i / 32) * nblk + j])) {
                     float C = vco_expcast_C(mnew);
                     float sig8 = 8.0f * sigma;
                     for (int kk = 0; kk < cnt; ++kk) code[kk] = vco_expcast_code(accv[kk], sig8, C);
@@ -574,7 +636,18 @@ int vco_attn(const uint8_t* Q8, const float* sq, const uint8_t* K8, const float*
         }
         free(Vd);
     }
+    free(flags);
     return 0;
+}
+
+int vco_attn(const uint8_t* Q8, const float* sq, const uint8_t* K8, const float* sk,
+             const uint8_t* V8T, const float* sv, const uint16_t* mu,
+             int B, int H, int N, int d, float kscale, int expcast, int vsmooth,
+             const int32_t* rows, int nrows, const float* acc_in,
+             double* O, uint8_t* P_out) {
+    if (expcast != 0 && expcast != 1) return 1;
+    return vco_attn_ex(Q8, sq, K8, sk, V8T, sv, mu, B, H, N, d, kscale, expcast, 0.0f, vsmooth,
+                       rows, nrows, acc_in, O, P_out);
 }
 
 /* ------------------------------------------------------------------ */

@@ -23,6 +23,10 @@ labels) with the block-fill permutation (vc_cluster_ex): grouping time, the
 relative error of the dequantized V', and the attention output against an
 fp64 reference on sampled query rows.
 
+--mode hybrid times the attention kernel with ExpCast bytes, exp-then-cast
+bytes and the hybrid bytes (exact exponent on high-weight tiles) at several
+margins, with the attention error against an fp64 reference on sampled rows.
+
 --impl reference times the CPU oracle (the only other implementation of the
 method that exists) on a bounded sample of the same workload.
 """
@@ -49,7 +53,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=5)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--mode", default="step", choices=["step", "schedule", "sweep", "preproc", "fill"])
+    ap.add_argument("--mode", default="step", choices=["step", "schedule", "sweep", "preproc", "fill", "hybrid"])
     ap.add_argument("--expcast", type=int, default=1)
     ap.add_argument("--vsmooth", type=int, default=1)
     ap.add_argument("--no-e2e", action="store_true")
@@ -562,14 +566,7 @@ def run_fill(args):
     g = torch.Generator(device="cpu").manual_seed(7)
     rows = torch.randperm(w.N, generator=g)[:256].to(dev)
     heads = list(range(0, H, max(1, H // 4)))[:4]
-    # fp64 reference rows, per sampled head
-    ref = {}
-    for h in heads:
-        q = Q[0, rows, h].double()
-        k = K[0, :, h].double()
-        v = V[0, :, h].double()
-        p = torch.softmax(q @ k.T / math.sqrt(w.d), dim=-1)
-        ref[h] = p @ v
+    ref = fp64_rows(Q, K, V, rows, heads, w.d)
     for fill in (0, 1):
         cent = cent0.clone()
         fn = lambda: vc.vc_cluster(V, w.k, 1, warm_start=True, centroids=cent.copy_(cent0), block_fill=fill)
@@ -607,6 +604,62 @@ def run_fill(args):
                    "sampled_rows": 256, "sampled_heads": heads}}), flush=True)
 
 
+def fp64_rows(Q, K, V, rows, heads, d):
+    """softmax(q K^T / sqrt d) V in fp64 (torch, on the device) for sampled rows."""
+    import torch
+    ref = {}
+    for h in heads:
+        q = Q[0, rows, h].double()
+        p = torch.softmax(q @ K[0, :, h].double().T / math.sqrt(d), dim=-1)
+        ref[h] = p @ V[0, :, h].double()
+    return ref
+
+
+def run_hybrid(args):
+    """Attention with ExpCast / exp-then-cast / hybrid bytes on the Wan2.2 shape:
+    kernel time and error against fp64 on sampled rows."""
+    import torch
+
+    from bit_fp8_attention_means_gb300 import inputs, vc
+    dev = torch.device("cuda", 0)
+    w = inputs.WORKLOADS["wan"]
+    H = args.heads or w.H
+    Q, K, V = inputs.make_qkv(w, dev, H=H)
+    perm = vc.vc_cluster(V, w.k, w.iters)[2]
+    qz = vc.vc_quantize(Q, K, V, perm, 1)
+    s = vc.shape_of(Q)
+    O = torch.empty_like(Q)
+    g = torch.Generator(device="cpu").manual_seed(7)
+    rows = torch.randperm(w.N, generator=g)[:256].to(dev)
+    heads = list(range(0, H, max(1, H // 4)))[:4]
+    ref = fp64_rows(Q, K, V, rows, heads, w.d)
+    flops = attn_flops(w.B, H, w.N, w.d)
+    arms = [("expcast", dict(expcast=1)), ("hybrid_m1", dict(exact_margin=1.0)),
+            ("hybrid_m2", dict(exact_margin=2.0)), ("hybrid_m3", dict(exact_margin=3.0)),
+            ("hybrid_m5", dict(exact_margin=5.0)), ("exp_then_cast", dict(expcast=0))]
+    out = []
+    for name, kw in arms:
+        fn = lambda: vc.vc_attn_fwd(qz, s, O=O, **kw)
+        for _ in range(max(2, args.warmup)):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = max(3, args.steps)
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        err = [float((O[0, rows, h].double() - ref[h]).norm() / ref[h].norm()) for h in heads]
+        out.append({"arm": name, **{k: v for k, v in kw.items()}, "ms": ms, "tflops": flops / (ms * 1e-3) / 1e12,
+                    "o_rel_err_vs_fp64": sum(err) / len(err)})
+    print(json.dumps({"mode": "hybrid", "metric": "attention kernel ms and O error vs fp64 per probability-byte mode",
+                      "rows": out,
+                      "config": {"workload": "wan2.2-shaped B=1 H=%d N=75600 d=128, vsmooth=1, k=256 pi" % H,
+                                 "sampled_rows": 256, "sampled_heads": heads}}), flush=True)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
@@ -620,6 +673,8 @@ def main():
         run_preproc(args)
     elif args.mode == "fill":
         run_fill(args)
+    elif args.mode == "hybrid":
+        run_hybrid(args)
     else:
         run_sweep(args)
 

@@ -142,7 +142,7 @@ static vc_status attn_common(const uint8_t* Q8, const float* sq, const uint8_t* 
                              int expcast, int vsmooth, void* O) {
     vc_status st = check_shape(shape);
     if (st != VC_OK) return st;
-    if ((expcast != 0 && expcast != 1) || (vsmooth != 0 && vsmooth != 1)) return VC_ERR_INVALID_ARG;
+    if ((expcast < 0 || expcast > 2) || (vsmooth != 0 && vsmooth != 1)) return VC_ERR_INVALID_ARG;
     if (!Q8 || !sq || !K8 || !sk || !V8T || !sv || !O || (vsmooth && !mu)) return VC_ERR_INVALID_ARG;
     if (!aligned16(Q8) || !aligned16(K8) || !aligned16(V8T) || !aligned16(O)) return VC_ERR_INVALID_ARG;
     return VC_OK;
@@ -151,17 +151,31 @@ static vc_status attn_common(const uint8_t* Q8, const float* sq, const uint8_t* 
 vc_status vc_attn_fwd(const uint8_t* Q8, const float* sq, const uint8_t* K8, const float* sk, const uint8_t* V8T,
                       const float* sv, const void* mu, vc_shape shape, float softmax_scale, int expcast, int vsmooth,
                       void* O, int32_t* dev_status, vc_stream_t stream) {
+    if (expcast != 0 && expcast != 1) return VC_ERR_INVALID_ARG;
     vc_status st = attn_common(Q8, sq, K8, sk, V8T, sv, mu, shape, expcast, vsmooth, O);
     if (st != VC_OK) return st;
-    return launch_attn(Q8, sq, K8, sk, V8T, sv, static_cast<const uint16_t*>(mu), shape, softmax_scale, expcast,
+    return launch_attn(Q8, sq, K8, sk, V8T, sv, static_cast<const uint16_t*>(mu), shape, softmax_scale, expcast, 0.f,
                        vsmooth, static_cast<uint16_t*>(O), dev_status, reinterpret_cast<cudaStream_t>(stream),
                        nullptr);
+}
+
+vc_status vc_attn_fwd_hybrid(const uint8_t* Q8, const float* sq, const uint8_t* K8, const float* sk,
+                             const uint8_t* V8T, const float* sv, const void* mu, vc_shape shape,
+                             float softmax_scale, float exact_margin, int vsmooth, void* O, int32_t* dev_status,
+                             vc_stream_t stream) {
+    if (exact_margin != exact_margin) return VC_ERR_INVALID_ARG;  // NaN
+    vc_status st = attn_common(Q8, sq, K8, sk, V8T, sv, mu, shape, 2, vsmooth, O);
+    if (st != VC_OK) return st;
+    return launch_attn(Q8, sq, K8, sk, V8T, sv, static_cast<const uint16_t*>(mu), shape, softmax_scale, 2,
+                       exact_margin, vsmooth, static_cast<uint16_t*>(O), dev_status,
+                       reinterpret_cast<cudaStream_t>(stream), nullptr);
 }
 
 vc_status vc_attn_fwd_debug(const uint8_t* Q8, const float* sq, const uint8_t* K8, const float* sk,
                             const uint8_t* V8T, const float* sv, const void* mu, vc_shape shape, float softmax_scale,
                             int expcast, int vsmooth, void* O, int32_t* dev_status, vc_stream_t stream, int dbg_bh,
-                            int dbg_qtile, float* S_dump, uint8_t* P_dump) {
+                            int dbg_qtile, float* S_dump, uint8_t* P_dump, float exact_margin) {
+    if (exact_margin != exact_margin) return VC_ERR_INVALID_ARG;
     vc_status st = attn_common(Q8, sq, K8, sk, V8T, sv, mu, shape, expcast, vsmooth, O);
     if (st != VC_OK) return st;
     if (!S_dump || !P_dump || dbg_bh < 0 || dbg_bh >= shape.B * shape.H || dbg_qtile < 0 ||
@@ -173,7 +187,8 @@ vc_status vc_attn_fwd_debug(const uint8_t* Q8, const float* sq, const uint8_t* K
     dbg.S = S_dump;
     dbg.P = P_dump;
     return launch_attn(Q8, sq, K8, sk, V8T, sv, static_cast<const uint16_t*>(mu), shape, softmax_scale, expcast,
-                       vsmooth, static_cast<uint16_t*>(O), dev_status, reinterpret_cast<cudaStream_t>(stream), &dbg);
+                       exact_margin, vsmooth, static_cast<uint16_t*>(O), dev_status,
+                       reinterpret_cast<cudaStream_t>(stream), &dbg);
 }
 
 }  // extern "C"

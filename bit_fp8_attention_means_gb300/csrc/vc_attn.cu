@@ -125,6 +125,7 @@ struct AttnParams {
     int H, N, nblk;
     int64_t Npad;
     float kscale;
+    float exact_margin;  // hybrid: a tile is exact if some row's tile max is within this of its running max (log2)
     int32_t* dev_status;
     uint64_t timeout_ns;
     int dbg_bh, dbg_qtile;
@@ -192,7 +193,9 @@ __device__ __forceinline__ float max64(const float (&a)[64]) {
     return max3(max3(u[0], u[1], u[2]), max3(u[3], u[4], u[5]), fmaxf(u[6], u[7]));
 }
 
-template <int D, bool EXPCAST, bool VSMOOTH, bool DBG>
+// EC: 0 exp-then-cast, 1 ExpCast, 2 hybrid (exp-then-cast on the key tiles
+// that are high-weight for the warp's 32 query rows, ExpCast elsewhere).
+template <int D, int EC, bool VSMOOTH, bool DBG>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
@@ -501,7 +504,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             const float sigma = __fmul_rn(__fmul_rn(sq_i, sk_j), p.kscale);
-            const float m_new = fmaxf(m, __fmul_rn(sigma, mx));
+            const float smx = __fmul_rn(sigma, mx);
+            const float m_new = fmaxf(m, smx);
+            // hybrid: the warp's 32 rows take exp-then-cast on this tile if one
+            // of its valid rows holds a probability >= 2^-margin of its running max
+            bool exact_tile = (EC == 0);
+            if constexpr (EC == 2)
+                exact_tile = __any_sync(0xffffffffu, qrow < p.N && __fsub_rn(smx, m_new) >= -p.exact_margin);
             const float alpha = ex2_approx(m - m_new);
             const float Cc = __fmaf_rn(-8.f, m_new, 119.65f);
             const float k1 = sigma * 0.0625f;
@@ -521,7 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (hf * 64 + i >= tail) a[i] = -INFINITY;
                 }
                 uint32_t pw[16];
-                if (EXPCAST) {
+                if (!exact_tile) {
                     if (fast) {
 #pragma unroll
                         for (int w = 0; w < 16; ++w) pw[w] = expcast4<false>(a + 4 * w, k1, k2);
@@ -665,7 +674,7 @@ bool make_map_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t ro
     return r == CUDA_SUCCESS;
 }
 
-template <int D, bool E, bool S, bool G>
+template <int D, int E, bool S, bool G>
 vc_status launch_one(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const AttnParams& p,
                      dim3 grid, cudaStream_t st) {
     auto kern = attn_fwd_kernel<D, E, S, G>;
@@ -679,21 +688,26 @@ vc_status launch_one(const CUtensorMap& mq, const CUtensorMap& mk, const CUtenso
     return cuda_status(cudaGetLastError());
 }
 
+template <int D, int E, bool G>
+vc_status launch_e(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const AttnParams& p,
+                   dim3 grid, cudaStream_t st, int vsmooth) {
+    return vsmooth ? launch_one<D, E, true, G>(mq, mk, mv, p, grid, st)
+                   : launch_one<D, E, false, G>(mq, mk, mv, p, grid, st);
+}
+
+template <int D, bool G>
+vc_status launch_g(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const AttnParams& p,
+                   dim3 grid, cudaStream_t st, int expcast, int vsmooth) {
+    if (expcast == 1) return launch_e<D, 1, G>(mq, mk, mv, p, grid, st, vsmooth);
+    if (expcast == 2) return launch_e<D, 2, G>(mq, mk, mv, p, grid, st, vsmooth);
+    return launch_e<D, 0, G>(mq, mk, mv, p, grid, st, vsmooth);
+}
+
 template <int D>
 vc_status launch_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const AttnParams& p,
                    dim3 grid, cudaStream_t st, int expcast, int vsmooth, bool dbg) {
-    if (dbg) {
-        if (expcast)
-            return vsmooth ? launch_one<D, true, true, true>(mq, mk, mv, p, grid, st)
-                           : launch_one<D, true, false, true>(mq, mk, mv, p, grid, st);
-        return vsmooth ? launch_one<D, false, true, true>(mq, mk, mv, p, grid, st)
-                       : launch_one<D, false, false, true>(mq, mk, mv, p, grid, st);
-    }
-    if (expcast)
-        return vsmooth ? launch_one<D, true, true, false>(mq, mk, mv, p, grid, st)
-                       : launch_one<D, true, false, false>(mq, mk, mv, p, grid, st);
-    return vsmooth ? launch_one<D, false, true, false>(mq, mk, mv, p, grid, st)
-                   : launch_one<D, false, false, false>(mq, mk, mv, p, grid, st);
+    return dbg ? launch_g<D, true>(mq, mk, mv, p, grid, st, expcast, vsmooth)
+               : launch_g<D, false>(mq, mk, mv, p, grid, st, expcast, vsmooth);
 }
 
 }  // namespace
@@ -713,7 +727,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_tiled_fn() {
 
 vc_status launch_attn(const uint8_t* Q8, const float* sq, const uint8_t* K8, const float* sk, const uint8_t* V8T,
                       const float* sv, const uint16_t* mu, const vc_shape& s, float softmax_scale, int expcast,
-                      int vsmooth, uint16_t* O, int32_t* dev_status, cudaStream_t st, const AttnDebug* dbg) {
+                      float exact_margin, int vsmooth, uint16_t* O, int32_t* dev_status, cudaStream_t st,
+                      const AttnDebug* dbg) {
     const int nblk = nblk_of(s.N);
     const int64_t Npad = npad_of(s.N);
     const uint64_t rows_qk = (uint64_t)s.B * s.H * Npad;
@@ -739,6 +754,7 @@ vc_status launch_attn(const uint8_t* Q8, const float* sq, const uint8_t* K8, con
     p.Npad = Npad;
     const double sc = softmax_scale > 0.f ? (double)softmax_scale : (double)(float)(1.0 / __builtin_sqrt((double)s.d));
     p.kscale = (float)(sc * 1.4426950408889634);
+    p.exact_margin = exact_margin;
     p.dev_status = dev_status;
     p.timeout_ns = 4000000000ull;
     p.dbg_bh = dbg ? dbg->bh : -1;

@@ -48,6 +48,7 @@ struct AttnDebug {
 };
 vc_status launch_attn(const uint8_t* Q8, const float* sq, const uint8_t* K8, const float* sk, const uint8_t* V8T,
                       const float* sv, const uint16_t* mu, const vc_shape& s, float softmax_scale, int expcast,
-                      int vsmooth, uint16_t* O, int32_t* dev_status, cudaStream_t st, const AttnDebug* dbg);
+                      float exact_margin, int vsmooth, uint16_t* O, int32_t* dev_status, cudaStream_t st,
+                      const AttnDebug* dbg);
 
 }  // namespace vc

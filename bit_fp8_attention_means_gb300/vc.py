@@ -66,8 +66,12 @@ def lib():
         L.vc_attn_fwd.restype = ctypes.c_int
         L.vc_attn_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, VcShape, ctypes.c_float, ctypes.c_int,
                                   ctypes.c_int, _vp, _vp, _vp]
+        L.vc_attn_fwd_hybrid.restype = ctypes.c_int
+        L.vc_attn_fwd_hybrid.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, VcShape, ctypes.c_float,
+                                         ctypes.c_float, ctypes.c_int, _vp, _vp, _vp]
         L.vc_attn_fwd_debug.restype = ctypes.c_int
-        L.vc_attn_fwd_debug.argtypes = L.vc_attn_fwd.argtypes + [ctypes.c_int, ctypes.c_int, _vp, _vp]
+        L.vc_attn_fwd_debug.argtypes = L.vc_attn_fwd.argtypes + [ctypes.c_int, ctypes.c_int, _vp, _vp,
+                                                                 ctypes.c_float]
         L.vc_debug_e4m3_encode.restype = ctypes.c_int
         L.vc_debug_e4m3_encode.argtypes = [_vp, ctypes.c_int64, _vp, _vp]
         L.vc_debug_wait_timeout.restype = ctypes.c_int
@@ -234,9 +238,12 @@ def quantize_staged_workspace_bytes(shape: VcShape) -> int:
 
 
 def vc_attn_fwd(qz, shape: VcShape, softmax_scale=0.0, expcast=1, vsmooth=1, O=None, dev_status=None,
-                stream=None, debug=None):
+                stream=None, debug=None, exact_margin=None):
     """FP8 attention on vc_quantize outputs. O is bf16 [B,N,H,d] laid out with `shape`'s strides.
 
+    exact_margin (float) selects the hybrid bytes (vc_attn_fwd_hybrid):
+    exp-then-cast on the key tiles within that many log2 units of a row's
+    running maximum, ExpCast elsewhere; expcast is then ignored.
     debug=(bh, qtile) additionally returns the fp32 scores and probability bytes
     of that one query tile: (O, S_dump [128, Npad], P_dump [128, Npad]).
     """
@@ -246,16 +253,22 @@ def vc_attn_fwd(qz, shape: VcShape, softmax_scale=0.0, expcast=1, vsmooth=1, O=N
         if (O.stride(0), O.stride(1), O.stride(2)) != (shape.s_b, shape.s_n, shape.s_h):
             O = torch.empty_strided((shape.B, shape.N, shape.H, shape.d), (shape.s_b, shape.s_n, shape.s_h, 1),
                                     dtype=torch.bfloat16, device=dev)
-    args = [_ptr(qz["Q8"]), _ptr(qz["sq"]), _ptr(qz["K8"]), _ptr(qz["sk"]), _ptr(qz["V8T"]), _ptr(qz["sv"]),
-            _ptr(qz["mu"]) if vsmooth else None, shape, float(softmax_scale), int(expcast), int(vsmooth), _ptr(O),
-            _ptr(dev_status), _stream(stream)]
+    ops = [_ptr(qz["Q8"]), _ptr(qz["sq"]), _ptr(qz["K8"]), _ptr(qz["sk"]), _ptr(qz["V8T"]), _ptr(qz["sv"]),
+           _ptr(qz["mu"]) if vsmooth else None, shape, float(softmax_scale)]
+    tail = [_ptr(O), _ptr(dev_status), _stream(stream)]
+    if exact_margin is not None:
+        expcast = 2
     if debug is None:
-        _check(lib().vc_attn_fwd(*args), "vc_attn_fwd")
+        if expcast == 2:
+            _check(lib().vc_attn_fwd_hybrid(*ops, float(exact_margin), int(vsmooth), *tail), "vc_attn_fwd_hybrid")
+        else:
+            _check(lib().vc_attn_fwd(*ops, int(expcast), int(vsmooth), *tail), "vc_attn_fwd")
         return O
     npad = nblk_of(shape.N) * BLOCK
     S = torch.zeros((BLOCK, npad), dtype=torch.float32, device=dev)
     P = torch.zeros((BLOCK, npad), dtype=torch.uint8, device=dev)
-    _check(lib().vc_attn_fwd_debug(*args, int(debug[0]), int(debug[1]), _ptr(S), _ptr(P)), "vc_attn_fwd_debug")
+    _check(lib().vc_attn_fwd_debug(*ops, int(expcast), int(vsmooth), *tail, int(debug[0]), int(debug[1]), _ptr(S),
+                                   _ptr(P), float(exact_margin or 0.0)), "vc_attn_fwd_debug")
     return O, S, P
 
 

@@ -281,18 +281,42 @@ vc_status vc_attn_fwd(const uint8_t* Q8, const float* sq, const uint8_t* K8, con
                       void* O, int32_t* dev_status, vc_stream_t stream);
 
 /*
+ * vc_attn_fwd with hybrid probability bytes: the exact exponent on the key
+ * tiles that carry high weight, ExpCast elsewhere.  The paper summary's own
+ * analysis (独立分析的弱点, weakness two) notes that ExpCast's fixed beta costs
+ * 0.7-2.1 dB and proposes keeping the exact exponent on high-weight tiles (a
+ * mixed-precision softmax).  This library's rule: query rows are taken in
+ * groups of 32 consecutive rows of a 128-row query tile (rows >= N do not
+ * count); key tile j is exact for a group if, for some row of it,
+ *   fl(sigma * max_k acc) - m' >= -exact_margin      (fp32, log2 units)
+ * i.e. the tile holds a probability >= 2^-exact_margin of that row's running
+ * maximum m'.  Exact tiles take the exp-then-cast byte of vc_attn_fwd with
+ * expcast = 0 for every row of the group, the others the ExpCast byte.
+ * exact_margin < 0 with |exact_margin| large gives vc_attn_fwd(expcast = 1),
+ * a large positive one vc_attn_fwd(expcast = 0).  Other arguments, layouts
+ * and errors as vc_attn_fwd; VC_ERR_INVALID_ARG for a NaN margin.
+ */
+vc_status vc_attn_fwd_hybrid(const uint8_t* Q8, const float* sq, const uint8_t* K8, const float* sk,
+                             const uint8_t* V8T, const float* sv, const void* mu, vc_shape shape,
+                             float softmax_scale, float exact_margin, int vsmooth,
+                             void* O, int32_t* dev_status, vc_stream_t stream);
+
+/*
  * Test hook for the ExpCast byte check: runs vc_attn_fwd and additionally,
  * for the single query tile `dbg_qtile` of head-slot `dbg_bh` (= b*H + h),
  * writes the fp32 scores acc it computed, S_dump fp32 [128, Npad], and the
  * probability bytes it fed to the PV product, P_dump uint8 [128, Npad]
  * (rows = the tile's 128 query rows, columns = keys in stored order).
- * Same contract as vc_attn_fwd otherwise; slower (a separate instantiation).
+ * expcast = 2 runs the hybrid bytes of vc_attn_fwd_hybrid with exact_margin
+ * (ignored for 0 and 1).  Same contract as vc_attn_fwd otherwise; slower (a
+ * separate instantiation).
  */
 vc_status vc_attn_fwd_debug(const uint8_t* Q8, const float* sq, const uint8_t* K8, const float* sk,
                             const uint8_t* V8T, const float* sv, const void* mu, vc_shape shape,
                             float softmax_scale, int expcast, int vsmooth,
                             void* O, int32_t* dev_status, vc_stream_t stream,
-                            int dbg_bh, int dbg_qtile, float* S_dump, uint8_t* P_dump);
+                            int dbg_bh, int dbg_qtile, float* S_dump, uint8_t* P_dump,
+                            float exact_margin);
 
 /*
  * Test hook: the device conversion the quantizer uses to write E4M3 codes

@@ -141,11 +141,11 @@ def test_cluster_cold_start(oracle_mod):
 
 # ---------------------------------------------------------------- attention
 
-def _pipeline(Q, K, V, k, iters, vsmooth, expcast, debug=None, use_cluster=True):
+def _pipeline(Q, K, V, k, iters, vsmooth, expcast, debug=None, use_cluster=True, margin=None):
     Qd, Kd, Vd = Q.to(DEV), K.to(DEV), V.to(DEV)
     perm = vc.vc_cluster(Vd, k, iters)[2] if use_cluster else None
     qz = vc.vc_quantize(Qd, Kd, Vd, perm, vsmooth)
-    res = vc.vc_attn_fwd(qz, vc.shape_of(Qd), expcast=expcast, vsmooth=vsmooth, debug=debug)
+    res = vc.vc_attn_fwd(qz, vc.shape_of(Qd), expcast=expcast, vsmooth=vsmooth, debug=debug, exact_margin=margin)
     torch.cuda.synchronize()
     return perm, qz, res
 
@@ -260,3 +260,64 @@ def test_invalid_arguments_raise():
     bad.d = 96
     with pytest.raises(vc.VcError):
         vc.vc_attn_fwd(qz, bad)
+
+
+# ---------------------------------------------------------------- hybrid bytes
+
+def _planted_peaky(N, d, H, seed):
+    """Queries sharing one direction b; the keys of tiles 0 and 3 aligned with
+    b, all other keys small noise: every row's running maximum is set in tile
+    0, tile 3 stays within ~1 of it, the other tiles ~8 (log2) below."""
+    g = torch.Generator().manual_seed(seed)
+    b = torch.randn(d, generator=g)
+    Q = torch.randn(1, N, H, d, generator=g) * 0.5 + b
+    K = torch.randn(1, N, H, d, generator=g) * 0.3
+    K[:, 0:128] += 0.5 * b
+    K[:, 384:512] += 0.5 * b
+    V = torch.randn(1, N, H, d, generator=g)
+    return tuple(t.to(torch.bfloat16) for t in (Q, K, V))
+
+
+@pytest.mark.parametrize("N,d,qtile", [(700, 64, 5), (1000, 128, 2), (1000, 128, 7)])
+def test_hybrid_bytes_match_oracle(oracle_mod, N, d, qtile):
+    """Hybrid mode: given the kernel's fp32 scores, the tiles the oracle writes
+    with ExpCast match bit for bit, the exp-then-cast tiles within one code."""
+    margin = 2.0
+    Q, K, V = _planted_peaky(N, d, 2, seed=17)
+    bh = 1
+    _, qz, (O, S, P) = _pipeline(Q, K, V, 8, 2, 1, 2, debug=(bh, qtile), margin=margin, use_cluster=False)
+    one = _slice_bh(_gpu_quant_np(qz), 0, bh)
+    rows = np.arange(qtile * 128, min(N, qtile * 128 + 128), dtype=np.int32)
+    acc = S.cpu().numpy()[: rows.size][None, None]
+    kw = dict(vsmooth=1, rows=rows, acc_in=acc, want_codes=True)
+    want_h = oracle_mod.attn(one, N, expcast=2, margin=margin, **kw)[1][0, 0]
+    want_1 = oracle_mod.attn(one, N, expcast=1, **kw)[1][0, 0]
+    want_0 = oracle_mod.attn(one, N, expcast=0, **kw)[1][0, 0]
+    got = P.cpu().numpy()[: rows.size]
+    diff = np.abs(got.astype(int) - want_h.astype(int))
+    assert diff.max() <= 1 and np.mean(diff == 0) > 0.999
+    nb = (N + 127) // 128
+    kinds = {}
+    for g in range(0, rows.size, 32):
+        for j in range(nb):
+            blk = np.s_[g:g + 32, 128 * j:128 * (j + 1)]
+            if np.array_equal(want_h[blk], want_1[blk]) and not np.array_equal(want_1[blk], want_0[blk]):
+                np.testing.assert_array_equal(got[blk], want_h[blk])   # an ExpCast tile: bit-exact
+                kinds[j] = "expcast"
+            elif not np.array_equal(want_h[blk], want_1[blk]):
+                kinds[j] = "exact"
+    # the planted pattern: tiles 0 and 3 exact, the rest ExpCast
+    assert kinds.get(0) == "exact" and kinds.get(3) == "exact", kinds
+    assert all(v == "expcast" for j, v in kinds.items() if j not in (0, 3)), kinds
+    assert sum(v == "expcast" for v in kinds.values()) >= 2, kinds
+
+
+@pytest.mark.parametrize("margin", [1.0, 3.0])
+def test_hybrid_attention_matches_oracle(oracle_mod, margin):
+    N, d = 1000, 128
+    Q, K, V = _case(N=N, d=d, H=2, seed=19)
+    _, qz, O = _pipeline(Q, K, V, 16, 2, 1, 2, margin=margin)
+    qn = _gpu_quant_np(qz)
+    ref = oracle_mod.attn(qn, N, expcast=2, margin=margin, vsmooth=1)
+    got = O.float().cpu().numpy().transpose(0, 2, 1, 3)
+    assert _rel(got, ref) <= O_TOL

@@ -321,7 +321,8 @@ def e2e_run(args, Q, K, V, run_on):
     hO = [torch.empty(Q.shape, dtype=Q.dtype).pin_memory() for _ in range(2)]
     bufs = [(Q, K, V, torch.empty_like(Q)), tuple(torch.empty_like(t) for t in (Q, K, V, Q))]
     comp = torch.cuda.current_stream()
-    cp = torch.cuda.Stream()
+    cp = torch.cuda.Stream()     # host -> device
+    cp_out = torch.cuda.Stream()  # device -> host (the link is full duplex)
     ev = lambda: torch.cuda.Event()
     ev_in, ev_done, ev_out = [ev(), ev()], [ev(), ev()], [ev(), ev()]
 
@@ -333,14 +334,15 @@ def e2e_run(args, Q, K, V, run_on):
             ev_in[b].record(cp)
 
     def d2h(b, O):
-        with torch.cuda.stream(cp):
-            cp.wait_event(ev_done[b])
+        with torch.cuda.stream(cp_out):
+            cp_out.wait_event(ev_done[b])
             hO[b].copy_(O, non_blocking=True)
-            ev_out[b].record(cp)
+            ev_out[b].record(cp_out)
 
     def run(steps, e0=None):
         if e0 is not None:
             cp.wait_event(e0)
+            cp_out.wait_event(e0)
         for b in range(2):
             ev_done[b].record(comp)
             ev_out[b].record(comp)
@@ -361,6 +363,16 @@ def e2e_run(args, Q, K, V, run_on):
 
     run(2)
     torch.cuda.synchronize()
+    # the link's own speed, for the record: one H2D of the inputs, one D2H of O
+    t0, t1, t2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+    t0.record(comp)
+    for dst, src in zip(bufs[0][:3], (hQ, hK, hV)):
+        dst.copy_(src, non_blocking=True)
+    t1.record(comp)
+    hO[0].copy_(bufs[0][3], non_blocking=True)
+    t2.record(comp)
+    torch.cuda.synchronize()
+    h2d_bytes, d2h_bytes = 3 * Q.numel() * Q.element_size(), Q.numel() * Q.element_size()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(comp)
     run(n_steps, e0)
@@ -369,8 +381,10 @@ def e2e_run(args, Q, K, V, run_on):
     ms = e0.elapsed_time(e1) / n_steps
     B, N, H, d = Q.shape
     return {"value": attn_flops(B, H, N, d) / (ms * 1e-3) / 1e12, "unit": "TFLOPS", "ms_per_step": ms,
-            "h2d_bytes_per_step": 3 * Q.numel() * Q.element_size(), "d2h_bytes_per_step": Q.numel() * Q.element_size(),
-            "steps": n_steps, "overlap": "H2D of step i+1 and D2H of step i on a copy stream during step i"}
+            "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes, "steps": n_steps,
+            "h2d_gbs": h2d_bytes / (t0.elapsed_time(t1) * 1e-3) / 1e9,
+            "d2h_gbs": d2h_bytes / (t1.elapsed_time(t2) * 1e-3) / 1e9,
+            "overlap": "H2D of step i+1 and D2H of step i on two copy streams during step i"}
 
 
 def run_reference(args):

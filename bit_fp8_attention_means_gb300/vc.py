@@ -259,7 +259,7 @@ def vc_attn_fwd(qz, shape: VcShape, softmax_scale=0.0, expcast=1, vsmooth=1, O=N
     if exact_margin is not None:
         expcast = 2
     if debug is None:
-        if expcast == 2:
+        if exact_margin is not None:
             _check(lib().vc_attn_fwd_hybrid(*ops, float(exact_margin), int(vsmooth), *tail), "vc_attn_fwd_hybrid")
         else:
             _check(lib().vc_attn_fwd(*ops, int(expcast), int(vsmooth), *tail), "vc_attn_fwd")

@@ -57,3 +57,14 @@ def test_attention_on_block_fill(oracle_mod):
     ref = oracle_mod.attn(want, 2000)
     got = O.float().cpu().numpy().transpose(0, 2, 1, 3)
     assert np.linalg.norm(got - ref) / np.linalg.norm(ref) <= 2e-3
+
+
+def test_block_fill_batched_warm(oracle_mod):
+    """B = 2, d = 64, warm start: the filled permutation of every (b, h)."""
+    w = inputs.WORKLOADS["tiny"]
+    _, _, V = inputs.make_qkv(w, DEV, B=2, H=3, N=2500, d=64)
+    cent, _, _ = vc.vc_cluster(V, 20, 3)
+    cent, lab, perm = vc.vc_cluster(V, 20, 1, warm_start=True, centroids=cent, block_fill=1)
+    torch.cuda.synchronize()
+    want = oracle_mod.block_fill(lab.cpu().numpy(), cent.cpu().numpy())
+    np.testing.assert_array_equal(perm.cpu().numpy(), want)

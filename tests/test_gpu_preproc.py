@@ -112,3 +112,23 @@ def test_wan_size_preproc(oracle_mod):
         ref = oracle_mod.attn(want, N, rows=rows)[0, 0]
         o = O[0, rows, h].float().cpu().numpy()
         assert np.linalg.norm(o - ref) / np.linalg.norm(ref) <= 2e-3
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_preproc_strided_batched(oracle_mod, d):
+    """Q/K/V as views into one [B, N, H, 3, d] buffer (strided heads), B = 2,
+    with a permutation: fused and unfused chains against the oracle."""
+    w = inputs.WORKLOADS["medium"]
+    B, N, H = 2, 900, 3
+    Q, K, V = inputs.make_qkv(w, "cpu", B=B, H=H, N=N, d=d, seed=23)
+    packed = torch.stack([Q, K, V], dim=3).to(DEV)
+    Qv, Kv, Vv = packed[:, :, :, 0], packed[:, :, :, 1], packed[:, :, :, 2]
+    g = torch.Generator().manual_seed(3)
+    perm = torch.stack([torch.stack([torch.randperm(N, generator=g) for _ in range(H)]) for _ in range(B)])
+    perm = perm.to(torch.int32)
+    rope = inputs.rope_table(N, d)
+    rope_d = torch.from_numpy(rope).to(DEV)
+    want = oracle_mod.quantize(u16(Q), u16(K), u16(V), perm.numpy(), 1, rope=rope, hadamard=1)
+    for fn in (vc.vc_quantize_ex, vc.vc_quantize_staged):
+        got = _np(fn(Qv, Kv, Vv, perm.to(DEV), 1, rope=rope_d, hadamard=1), 1)
+        _assert_same(got, want, 1, fn.__name__)

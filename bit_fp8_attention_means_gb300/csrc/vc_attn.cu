@@ -106,7 +106,9 @@ struct Cfg {
     static constexpr int B_SE = B_OD + 2;        // [2] row sum read back, S_X free (4 warps)
     static constexpr int B_OF = B_SE + 2;        // [2] last mean restore of tile X complete
     static constexpr int B_TD = B_OF + 2;        // [2] every MMA of tile X's issuer complete
-    static constexpr int NBAR_USED = B_TD + 2;
+    static constexpr int B_AMF = B_TD + 2;       // [2] mean-restore A operand of tile X written (4 warps)
+    static constexpr int B_MD = B_AMF + 2;       // [2] mean-restore MMA of tile X complete
+    static constexpr int NBAR_USED = B_MD + 2;
     static_assert(NBAR_USED <= NBAR, "barrier area");
     // TMEM columns
     __host__ __device__ static constexpr uint32_t base(int X) { return (uint32_t)X * (D + 128); }
@@ -235,6 +237,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(C::B_SE + X), 4);
             mbar_init(bar(C::B_OF + X), 1);
             mbar_init(bar(C::B_TD + X), 1);
+            mbar_init(bar(C::B_AMF + X), 4);
+            mbar_init(bar(C::B_MD + X), 1);
         }
         *abort_flag = 0;
         fence_barrier_init();
@@ -393,15 +397,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
-                    if (VSMOOTH && (j - 1) % kBatch == kBatch - 1) {
-                        tc_fence_after();
-                        issue_mean((j - 1) / kBatch);
-                    }
                 }
                 tc_fence_after();
                 issue_qk(j);
                 mma_commit_w(bar(C::B_SF + X));
                 mma_commit_w(bar(C::B_KE + j % NSK));
+                if (VSMOOTH && j > 0 && (j - 1) % kBatch == kBatch - 1) {
+                    // the batch that ended with tile j-1: its row-sum operand is
+                    // written after S_X was released, and the softmax of tile j
+                    // waits for this product before it rescales O
+                    const int bi = (j - 1) / kBatch;
+                    if (!mbar_wait_warp(bar(C::B_AMF + X), bi & 1, abort_flag, p.dev_status, tmo)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    issue_mean(bi);
+                    mma_commit_w(bar(C::B_MD + X));
+                }
                 if (!mbar_wait_warp(bar(C::B_VF + j % NSV), (j / NSV) & 1, abort_flag, p.dev_status, tmo) ||
                     !mbar_wait_warp(bar(C::B_PF + X), j & 1, abort_flag, p.dev_status, tmo)) {
                     ok = false;
@@ -417,7 +430,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
             }
-            if (ok && mbar_wait_warp(bar(C::B_SE + X), (J - 1) & 1, abort_flag, p.dev_status, tmo)) {
+            if (ok && mbar_wait_warp(bar(C::B_SE + X), (J - 1) & 1, abort_flag, p.dev_status, tmo) &&
+                (!VSMOOTH || mbar_wait_warp(bar(C::B_AMF + X), ((J - 1) / kBatch) & 1, abort_flag, p.dev_status, tmo))) {
                 tc_fence_after();
                 if (VSMOOTH) issue_mean((J - 1) / kBatch);
                 mma_commit_w(bar(C::B_OF + X));
@@ -571,9 +585,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             tmem_wait_st();
-            // O holds every product up to tile j-1 (and any mean restore): the
-            // completion of the P V of tile j-1 and of the QK^T of tile j were
-            // both observed above.
+            // O holds every product up to tile j-1: the completion of the P V of
+            // tile j-1 and of the QK^T of tile j were both observed above; the
+            // mean restore of the batch that ended with tile j-1 is issued after
+            // this QK^T, so its completion is awaited here
+            if (VSMOOTH && j > 0 && slot == 0) {
+                if (!mbar_wait_warp(bar(C::B_MD + X), ((j - 1) / kBatch) & 1, abort_flag, p.dev_status, tmo))
+                    return false;
+                tc_fence_after();
+            }
             if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
                 for (int c0 = 0; c0 < D; c0 += 32) {
@@ -606,11 +626,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (VSMOOTH) {
                 hist[slot * 128] = r;
                 hist[(kBatch + slot) * 128] = m_new;
-                if (slot == kBatch - 1 || LAST) close_batch(m_new, slot + 1);
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(C::B_SE + X));
+            // the batch's row-sum operand is built after S_X is released, off
+            // the path to the next QK^T
+            if (VSMOOTH && (slot == kBatch - 1 || LAST)) {
+                close_batch(m_new, slot + 1);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(C::B_AMF + X));
+            }
             return true;
         };
 

@@ -586,15 +586,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tmem_wait_st();
             // O holds every product up to tile j-1: the completion of the P V of
-            // tile j-1 and of the QK^T of tile j were both observed above; the
+            // tile j-1 and of the QK^T of tile j were both observed above.  The
             // mean restore of the batch that ended with tile j-1 is issued after
-            // this QK^T, so its completion is awaited here
-            if (VSMOOTH && j > 0 && slot == 0) {
-                if (!mbar_wait_warp(bar(C::B_MD + X), ((j - 1) / kBatch) & 1, abort_flag, p.dev_status, tmo))
-                    return false;
-                tc_fence_after();
-            }
+            // this QK^T, so a rescale here first awaits it; without a rescale
+            // nothing touches O before this tile's P V, which the MMA warp
+            // issues after the mean MMA, and the next QK^T's commit covers it
             if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                if (VSMOOTH && slot == 0) {
+                    if (!mbar_wait_warp(bar(C::B_MD + X), ((j - 1) / kBatch) & 1, abort_flag, p.dev_status, tmo))
+                        return false;
+                    tc_fence_after();
+                }
 #pragma unroll
                 for (int c0 = 0; c0 < D; c0 += 32) {
                     uint32_t o[32];

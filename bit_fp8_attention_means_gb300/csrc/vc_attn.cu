@@ -302,40 +302,67 @@ __global__ void __launch_bounds__(kThreads, 1)
             ginv[e] = __frcp_rn(sv > 0.f ? sv : 1.f);
         }
         if (lane == 0) prefetch_tensormap(&tmV);
+        // Mean operand of batch bt (key tiles 16 bt .. 16 bt + 15) into buffer
+        // bt & 1: for channel n the 48 bf16 at k = 3t, 3t+1, 3t+2 hold
+        // (mu'_hi, mu'_hi, mu'_lo) of tile t, mu' = mu / g; tiles past the
+        // last are 0.  Written in halves of 8 tiles (3 chunks of 16 bytes per
+        // channel each), with one proxy fence per batch.
+        auto write_batch = [&](int bt) {
+            uint8_t* bmb = smem + C::OFF_BM + (bt & 1) * C::BMB;
+#pragma unroll
+            for (int hb = 0; hb < 2; ++hb) {
+                uint32_t mw[8][PER / 2];
+#pragma unroll
+                for (int t = 0; t < 8; ++t) {
+                    const int jt = bt * kBatch + hb * 8 + t;
+                    const uint32_t* src =
+                        reinterpret_cast<const uint32_t*>(p.mu + ((int64_t)bh * p.nblk + jt) * D + lane * PER);
+#pragma unroll
+                    for (int e = 0; e < PER / 2; ++e) mw[t][e] = (jt < J) ? __ldg(src + e) : 0u;
+                }
+#pragma unroll
+                for (int e = 0; e < PER; ++e) {
+                    uint16_t v[24];  // k = 24 hb .. 24 hb + 23
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) {
+                        const uint32_t bits = (e & 1) ? (mw[t][e / 2] >> 16) : (mw[t][e / 2] & 0xFFFFu);
+                        const float mp = __fmul_rn(bf16_bits_to_f32(bits), ginv[e]);
+                        const uint16_t hi = bf16_rn_bits(mp);
+                        const uint16_t lo = bf16_rn_bits(__fsub_rn(mp, bf16_bits_to_f32(hi)));
+                        v[3 * t] = hi;
+                        v[3 * t + 1] = hi;
+                        v[3 * t + 2] = lo;
+                    }
+                    const int n_ch = lane * PER + e;
+#pragma unroll
+                    for (int c = 0; c < 3; ++c) {
+                        uint32_t w4[4];
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) w4[q] = (uint32_t)v[8 * c + 2 * q] | ((uint32_t)v[8 * c + 2 * q + 1] << 16);
+                        *reinterpret_cast<uint4*>(bmb + mo_offset(n_ch, 24 * hb + 8 * c)) =
+                            make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                    }
+                }
+            }
+            fence_proxy_async_smem();  // the generic-proxy writes above are read by the MMAs
+        };
         int issued = 0;
         for (int j = 0; j < J; ++j) {
             const int s = j % NSV;
-            // the block mean goes out before the wait for a free stage, so its
-            // latency overlaps it
-            uint32_t mu_w[PER / 2];
-            if (VSMOOTH) {
-                const uint32_t* src =
-                    reinterpret_cast<const uint32_t*>(p.mu + ((int64_t)bh * p.nblk + j) * D + lane * PER);
-#pragma unroll
-                for (int e = 0; e < PER / 2; ++e) mu_w[e] = __ldg(src + e);
-            }
             if (j >= NSV && !mbar_wait_warp(bar(C::B_VE + s), (j / NSV - 1) & 1, abort_flag, p.dev_status, tmo))
                 break;
             if (lane == 0) {
                 mbar_expect_tx(bar(C::B_VF + s), D * 128);
                 tma_load_2d(sbase + C::OFF_V + s * C::VB, &tmV, j * 128, bh * D, bar(C::B_VF + s));
             }
+            // Batch 0 goes out with tile 0, batch b+1 with tile 16 b + 8: by then
+            // the V stage of tile 16 b + 5 has been released, so both tiles' P V
+            // up to it -- and the mean MMA of batch b-1 issued before them, the
+            // last reader of buffer (b+1) & 1 -- have completed.  The batch's own
+            // mean MMA comes after the MMA warp has waited for this stage.
             if (VSMOOTH) {
-                // mean operand rows: k = 3t, 3t+1, 3t+2 hold (mu'_hi, mu'_hi, mu'_lo), mu' = mu / g
-                uint8_t* bmb = smem + C::OFF_BM + ((j / kBatch) & 1) * C::BMB;
-                const int k0 = 3 * (j % kBatch);
-#pragma unroll
-                for (int e = 0; e < PER; ++e) {
-                    const int n_ch = lane * PER + e;
-                    const uint32_t bits = (e & 1) ? (mu_w[e / 2] >> 16) : (mu_w[e / 2] & 0xFFFFu);
-                    const float mp = __fmul_rn(bf16_bits_to_f32(bits), ginv[e]);
-                    const uint16_t hi = bf16_rn_bits(mp);
-                    const uint16_t lo = bf16_rn_bits(__fsub_rn(mp, bf16_bits_to_f32(hi)));
-                    *reinterpret_cast<uint16_t*>(bmb + mo_offset(n_ch, k0)) = hi;
-                    *reinterpret_cast<uint16_t*>(bmb + mo_offset(n_ch, k0 + 1)) = hi;
-                    *reinterpret_cast<uint16_t*>(bmb + mo_offset(n_ch, k0 + 2)) = lo;
-                }
-                fence_proxy_async_smem();  // the generic-proxy writes above are read by the MMAs
+                if (j == 0) write_batch(0);
+                else if (j % kBatch == kBatch / 2 && (j / kBatch + 1) * kBatch < J) write_batch(j / kBatch + 1);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(C::B_VF + s));
@@ -349,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // instruction is issued by one elected lane.  Per key tile j: QK^T into
         // S_X once the softmax has released it, then P V (+ row sum) once the
         // probability bytes are in place.  The batch's mean restore goes in
-        // right after the release that closes the batch, ahead of the next QK^T.
+        // after the next QK^T, once the softmax has written its operand.
         const int X = warp - kMmaWarp0;
         const uint32_t tb = tmem + C::base(X);
         {

@@ -476,13 +476,20 @@ __device__ __forceinline__ int stage_v_block(const VArgs& a, int b, int h, int j
     }
     __syncthreads();
     const uint16_t* base = a.V + (int64_t)b * a.s_b + (int64_t)h * a.s_h;
-    constexpr int CH = D / 8;  // 16-byte chunks per row
-#pragma unroll 4
-    for (int e = threadIdx.x; e < kBlock * CH; e += kVThreads) {
+    constexpr int CH = D / 8;                     // 16-byte chunks per row
+    constexpr int PER = kBlock * CH / kVThreads;  // chunks per thread: all loads in flight, then the stores
+    uint4 w[PER];
+#pragma unroll
+    for (int r = 0; r < PER; ++r) {
+        const int e = threadIdx.x + r * kVThreads;
         const int t = e / CH, q = e % CH;
-        uint4 w = make_uint4(0, 0, 0, 0);
-        if (t < cnt) w = __ldg(reinterpret_cast<const uint4*>(base + (int64_t)src_s[t] * a.s_n) + q);
-        *reinterpret_cast<uint4*>(vs + t * D + q * 8) = w;
+        w[r] = (t < cnt) ? __ldg(reinterpret_cast<const uint4*>(base + (int64_t)src_s[t] * a.s_n) + q)
+                         : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int r = 0; r < PER; ++r) {
+        const int e = threadIdx.x + r * kVThreads;
+        *reinterpret_cast<uint4*>(vs + (e / CH) * D + (e % CH) * 8) = w[r];
     }
     __syncthreads();
     return cnt;

@@ -5,8 +5,9 @@
 //   Q, K' = K[pi]: one fp32 scale per 128-token block, codes = E4M3(x * 448/amax).
 //   V' = V[pi]:   mu_j = bf16(block mean), R = V' - mu_j, residual codes with
 //                 one scale per channel over the whole head.
-// Three memory-bound kernels per call:
-//   quant_qk_kernel      Q and K' blocks (gathered rows for K'), one CTA per block.
+// vc_quantize: three memory-bound kernels per call:
+//   quant_qk_kernel      Q and K' blocks (gathered rows for K'), one CTA per
+//                        (head, block), heads fastest.
 //   quant_v_stats_kernel block means of V' and the per-channel residual amax
 //                        (atomicMax on the fp32 bit pattern, values are >= 0).
 //   quant_v_codes_kernel residual codes, written token-contiguous per channel
@@ -14,6 +15,12 @@
 //                        read V as a K-major MMA operand.
 // The two V kernels stage each block's gathered rows in shared memory with
 // 16-byte loads; the per-channel scale needs the whole head, hence two passes.
+// vc_quantize_ex replaces quant_qk_kernel with quant_qk_pre_kernel, which
+// also applies the rotary transform and the Hadamard rotation to Q and K'
+// (the rest of the pages' fused preprocessing chain: paper summary 核心方法,
+// dimensionstp.github.io 3-1 and 3-3); vc_quantize_staged runs the same
+// computation as separate kernels with fp32 intermediates (rope_stage,
+// gather_stage, hadamard_stage, then the quantizers) to measure the fusion.
 // Every rounding step is written with an explicit _rn intrinsic so that the
 // codes are bit-reproducible: fp32 block sum in token order, IEEE division,
 // round-to-nearest-even conversions (cvt.rn.satfinite.e4m3x2).

@@ -439,10 +439,14 @@ __global__ void __launch_bounds__(kAsThreads, 1)
             *reinterpret_cast<uint4*>(smem + C::OFF_C + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
             *reinterpret_cast<uint4*>(smem + C::OFF_C + C::CPART + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
-        for (int c = threadIdx.x; c < kpad; c += kAsThreads) {
-            float acc = 0.f;
-            if (c < k)
+        // |c|^2 for the real centroids, +inf for the padding up to kAsMaxK, so
+        // that a padded column can never be the minimum
+        for (int c = threadIdx.x; c < kAsMaxK; c += kAsThreads) {
+            float acc = INFINITY;
+            if (c < k) {
+                acc = 0.f;
                 for (int e = 0; e < D; ++e) acc = __fmaf_rn(cb[(int64_t)c * D + e], cb[(int64_t)c * D + e], acc);
+            }
             cn_s[c] = acc;
         }
         fence_proxy_async_smem();
@@ -504,27 +508,50 @@ __global__ void __launch_bounds__(kAsThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                float best = INFINITY;
-                int arg = 0;
-                for (int c0 = 0; c0 < kpad; c0 += 16) {
-                    uint32_t r[16];
-                    tmem_ld16(lane_addr + buf * 256 + c0, r);
+                // 64 columns per TMEM round trip; four independent running minima
+                // (columns c = 4i + q), each keeping its first minimum, merged at
+                // the end with ties to the lower column: the same argmin as one
+                // pass in column order.  Columns past k (stale TMEM past kpad
+                // included) meet |c|^2 = +inf and never win.
+                float best[4] = {INFINITY, INFINITY, INFINITY, INFINITY};
+                int arg[4] = {0, 0, 0, 0};
+                const float4* cn4 = reinterpret_cast<const float4*>(cn_s);
+                for (int c0 = 0; c0 < kpad; c0 += 64) {
+                    uint32_t r[64];
+                    tmem_ld32(lane_addr + buf * 256 + c0, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+                    if (c0 + 32 < kpad) tmem_ld32(lane_addr + buf * 256 + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
                     tmem_wait_ld();
+                    const int nq = (c0 + 32 < kpad) ? 16 : 8;  // float4 groups of columns in this round
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const int c = c0 + e;
-                        const float dist = __fmaf_rn(-2.f, __uint_as_float(r[e]), cn_s[c]);
-                        if (c < k && dist < best) {
-                            best = dist;
-                            arg = c;
+                    for (int g = 0; g < 16; ++g) {
+                        if (g < nq) {
+                            const float4 cn = cn4[(c0 >> 2) + g];
+                            const float cv[4] = {cn.x, cn.y, cn.z, cn.w};
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                const float dist = __fmaf_rn(-2.f, __uint_as_float(r[4 * g + q]), cv[q]);
+                                if (dist < best[q]) {
+                                    best[q] = dist;
+                                    arg[q] = c0 + 4 * g + q;
+                                }
+                            }
                         }
                     }
                 }
+                float bestv = best[0];
+                int argv = arg[0];
+#pragma unroll
+                for (int q = 1; q < 4; ++q)
+                    if (best[q] < bestv || (best[q] == bestv && arg[q] < argv)) {
+                        bestv = best[q];
+                        argv = arg[q];
+                    }
+                const int arg_final = argv;
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(C::B_DE + buf));
                 const int t = (seg + i - bh * tiles_per_head) * 128 + row;
-                if (t < s.N) labels[(int64_t)bh * s.N + t] = arg;
+                if (t < s.N) labels[(int64_t)bh * s.N + t] = arg_final;
             }
         }
         // every role has finished this head's tiles (the epilogue waited for the

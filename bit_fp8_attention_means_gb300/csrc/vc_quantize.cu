@@ -186,23 +186,24 @@ __global__ void __launch_bounds__(kQkThreads) quant_qk_kernel(QkArgs q, QkArgs k
 // ------------------------------------------------------------------ fused rotary + Hadamard
 //
 // Q/K block quantizer with the rotary transform and the Hadamard rotation in
-// registers.  Persistent: one CTA of 512 threads per SM walks the (tensor,
-// batch, block, head) tiles, heads fastest so that the CTAs running at the same
-// time share the rows of the rotary table, and stages every tile in shared
-// memory with 16-byte cp.async copies one tile ahead: the copies of tile i+1
-// (the gathered bf16 rows and their table rows) run while tile i is computed;
-// the perm entries are loaded a further tile ahead.  Four threads per token
-// row, each holding D/4 channels: warp w computes rows 8w .. 8w+7 and also
-// copies them (lane l holds the source index of row 8w + (l & 7) and hands it
-// out by shuffle), whole rows per instruction so that every sector is read
-// once.  Shared rows are stored with a row- and quarter-dependent rotation of
-// the 16-byte chunks inside each group of 8, so that the compute reads (eight
-// lanes = two rows x four quarters per phase) are free of bank conflicts.
+// registers.  Persistent: one CTA of 128 * kPreTpr threads per SM walks the
+// (tensor, batch, block, head) tiles, heads fastest so that the CTAs running
+// at the same time share the rows of the rotary table, and stages every tile
+// in shared memory with 16-byte cp.async copies one tile ahead: the copies of
+// tile i+1 (the gathered bf16 rows and their table rows) run while tile i is
+// computed; the perm entries are loaded a further tile ahead.  kPreTpr
+// threads per token row, each holding D/kPreTpr channels (2 and D/2 here; 4
+// measured the same): warp w computes rows (32/kPreTpr) w .. and also copies
+// them (lane l holds the source index of one of them and hands it out by
+// shuffle), whole rows per instruction so that every sector is read once.
+// Shared rows are stored with a row- and part-dependent rotation of the
+// 16-byte chunks inside each group of 8, so that the compute reads (the eight
+// lanes of a shared-memory phase) are free of bank conflicts.
 // Arithmetic is that of the plain path plus, per row: rotation of each channel
 // pair (four products, then difference and sum) and the Walsh-Hadamard stages
-// of stride 1 .. D/8 in the thread, D/4 and D/2 across lanes (xor 1, xor 2),
-// each result rounded as the definition states; packed fp32 instructions carry
-// two of them at once.
+// of stride 1 .. D/(2 kPreTpr) in the thread and D/kPreTpr .. D/2 across the
+// row's lanes, each result rounded as the definition states; packed fp32
+// instructions carry two of them at once.
 
 constexpr int kPreTpr = 2;                    // threads per token row
 constexpr int kPreThreads = kBlock * kPreTpr;

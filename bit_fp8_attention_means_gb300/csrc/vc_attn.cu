@@ -40,6 +40,11 @@
 // residual is identically 0; mu' = mu * fp32(1/g_c)), so O = g (.) A / l at
 // the end.
 //
+// The row max of a key tile comes from the TMEM loads themselves
+// (tcgen05.ld.red with max: each 32-column load also returns the maximum of
+// this lane's 32 values), so the first read costs four loads and three max
+// instructions; only the last, masked tile reduces in registers.
+//
 // ExpCast inner loop, per score: ts = sat(acc * sigma/16 + C/128) (one FFMA
 // with saturation = clip to [0, 128] of t/128, exact because /128 and /16 are
 // powers of two), then b = ts*128 + 1.5*2^23 (packed FFMA2) whose low byte is
@@ -181,6 +186,19 @@ __device__ __forceinline__ void load_half(uint32_t taddr, float (&a)[64]) {
         a[i] = __uint_as_float(r0[i]);
         a[32 + i] = __uint_as_float(r1[i]);
     }
+}
+
+// 32 columns of this thread's TMEM lane and their maximum (tcgen05.ld.red).
+__device__ __forceinline__ void tmem_ld32_max(uint32_t taddr, uint32_t (&r)[32], float& mx) {
+    asm volatile(
+        "tcgen05.ld.red.sync.aligned.32x32b.x32.max.f32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, %32, [%33];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]),
+          "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+          "=r"(r[30]), "=r"(r[31]), "=f"(mx)
+        : "r"(taddr));
 }
 
 __device__ __forceinline__ float max64(const float (&a)[64]) {
@@ -525,7 +543,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             // first read: the row max over all 128 keys
             float mx;
-            {
+            if (!masked) {
+                // the loads reduce as they read: the row max comes with the data
+                uint32_t r0[32], r1[32], r2[32], r3[32];
+                float m0, m1, m2, m3;
+                tmem_ld32_max(lane_addr + C::COL_S, r0, m0);
+                tmem_ld32_max(lane_addr + C::COL_S + 32, r1, m1);
+                tmem_ld32_max(lane_addr + C::COL_S + 64, r2, m2);
+                tmem_ld32_max(lane_addr + C::COL_S + 96, r3, m3);
+                tmem_wait_ld();
+                mx = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+                if (dbg_cta) {
+                    float* dst = p.S_dump + (int64_t)row * p.Npad + j * 128;
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        dst[i] = __uint_as_float(r0[i]);
+                        dst[32 + i] = __uint_as_float(r1[i]);
+                        dst[64 + i] = __uint_as_float(r2[i]);
+                        dst[96 + i] = __uint_as_float(r3[i]);
+                    }
+                }
+            } else {
                 float a[64];
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {

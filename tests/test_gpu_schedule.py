@@ -1,0 +1,48 @@
+"""The amortized grouping schedule on the device, against the oracle.
+
+Paper summary (paper.rainbus.top), 方法步骤详情 step 1: cluster in the first
+quarter of the steps (warm-started), reuse pi in between.  Over 6 steps of a
+20-step run with V drifting between steps, the state after the warm
+clustering at step 4 still yields pi = stable argsort of its labels, and the
+reuse step 5 (new Q, K, V, the step-4 pi) quantizes bit-exactly and attends
+within 2e-3 of the oracle on that pi.
+"""
+import numpy as np
+import pytest
+import torch
+
+from bit_fp8_attention_means_gb300 import inputs, schedule, vc
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+u16 = inputs.to_u16
+
+
+def test_schedule_reuse_step_matches_oracle(oracle_mod):
+    w = inputs.WORKLOADS["tiny"]
+    N, d, H, k = 1000, 64, 2, 8
+    Q, K, V = inputs.make_qkv(w, "cpu", H=H, N=N, d=d, seed=41)
+    g = torch.Generator().manual_seed(7)
+    st = schedule.GroupingState()
+    qz = O = None
+    for s in range(6):
+        if s:
+            V = (V.float() + 0.05 ** 0.5 * torch.randn(V.shape, generator=g)).to(torch.bfloat16)
+            Q = torch.randn(Q.shape, generator=g).to(torch.bfloat16)
+            K = torch.randn(K.shape, generator=g).to(torch.bfloat16)
+        Qd, Kd, Vd = Q.to(DEV), K.to(DEV), V.to(DEV)
+        qz, O = schedule.run_step(st, Qd, Kd, Vd, s, 20, k, cold_iters=5, warm_iters=1, qz=qz, O=O)
+        torch.cuda.synchronize()
+        if s == 4:
+            assert st.clusterings == 2
+            np.testing.assert_array_equal(st.perm.cpu().numpy(),
+                                          oracle_mod.argsort_labels(st.labels.cpu().numpy(), k))
+            perm4 = st.perm.clone()
+    assert st.clusterings == 2 and torch.equal(st.perm, perm4)
+    want = oracle_mod.quantize(u16(Q), u16(K), u16(V), perm4.cpu().numpy(), 1)
+    for key in ("Q8", "sq", "K8", "sk", "V8T", "sv"):
+        np.testing.assert_array_equal(qz[key].cpu().numpy(), want[key], err_msg=key)
+    np.testing.assert_array_equal(qz["mu"].cpu().numpy().view(np.uint16), want["mu"])
+    ref = oracle_mod.attn(want, N)
+    got = O.float().cpu().numpy().transpose(0, 2, 1, 3)
+    assert np.linalg.norm(got - ref) / np.linalg.norm(ref) <= 2e-3

@@ -1,0 +1,92 @@
+"""Host logic of the amortized grouping schedule (no GPU).
+
+Paper summary (paper.rainbus.top), 方法步骤详情 step 1: cluster only in the
+first quarter of the denoising steps, warm-started from the previous
+centroids, and reuse a permutation for 4 neighbouring steps.  The checks:
+
+* the steps that cluster, for step counts where the ceiling matters;
+* a step sequence through ``run_step`` with the library calls replaced by a
+  recorder: the first clustering is cold, later ones warm from the centroids
+  the previous one returned, every other step quantizes with the last pi,
+  ``vsmooth = 0`` never clusters and quantizes with the identity.
+"""
+import math
+
+import pytest
+
+from bit_fp8_attention_means_gb300 import schedule
+
+
+@pytest.mark.parametrize("S,want", [(50, [0, 4, 8, 12]), (4, [0]), (1, [0]), (16, [0]),
+                                    (17, [0, 4]), (20, [0, 4]), (33, [0, 4, 8]), (0, [])])
+def test_clustering_steps(S, want):
+    got = [s for s in range(S) if schedule.clusters_at(s, S)]
+    assert got == want
+    # every clustering step lies in the first quarter, rounded up
+    assert all(s < math.ceil(0.25 * S) for s in got)
+
+
+class _Recorder:
+    """Stands in for the binding: records each call and returns tokens."""
+
+    def __init__(self):
+        self.calls = []
+        self.n = 0
+
+    def vc_cluster(self, V, k, iters, warm_start=False, centroids=None, labels=None, perm=None,
+                   workspace=None, stream=None):
+        self.n += 1
+        self.calls.append(("cluster", iters, warm_start, centroids))
+        return ("C%d" % self.n, "z%d" % self.n, "pi%d" % self.n)
+
+    def vc_quantize(self, Q, K, V, perm, vsmooth, out=None, stream=None):
+        self.calls.append(("quantize", perm, vsmooth))
+        return "qz"
+
+    def vc_attn_fwd(self, qz, shape, expcast=1, vsmooth=1, O=None, stream=None):
+        self.calls.append(("attn", expcast, vsmooth))
+        return "O"
+
+    def shape_of(self, Q):
+        return None
+
+
+def _run(monkeypatch, S, vsmooth=1):
+    rec = _Recorder()
+    monkeypatch.setattr(schedule, "vc", rec)
+    st = schedule.GroupingState()
+    for s in range(S):
+        schedule.run_step(st, "Q", "K", "V", s, S, k=8, cold_iters=5, warm_iters=1, vsmooth=vsmooth,
+                          stream=object())
+    return rec, st
+
+
+def test_step_sequence_cold_then_warm(monkeypatch):
+    rec, st = _run(monkeypatch, 50)
+    clus = [c for c in rec.calls if c[0] == "cluster"]
+    assert [c[1:3] for c in clus] == [(5, False), (1, True), (1, True), (1, True)]
+    # each warm start takes the centroids the previous clustering returned
+    assert [c[3] for c in clus] == [None, "C1", "C2", "C3"]
+    assert st.clusterings == 4 and st.perm == "pi4"
+    # the permutation each step quantizes with: the last one computed
+    perms = [c[1] for c in rec.calls if c[0] == "quantize"]
+    want = ["pi%d" % (min(s // 4, 3) + 1) for s in range(50)]
+    assert perms == want
+    assert sum(c[0] == "attn" for c in rec.calls) == 50
+
+
+def test_vsmooth_off_never_clusters(monkeypatch):
+    rec, st = _run(monkeypatch, 12, vsmooth=0)
+    assert not [c for c in rec.calls if c[0] == "cluster"]
+    assert all(c[1] is None and c[2] == 0 for c in rec.calls if c[0] == "quantize")
+    assert st.clusterings == 0
+
+
+def test_missing_permutation_forces_a_clustering(monkeypatch):
+    """A state with no pi yet clusters even on a reuse step."""
+    rec = _Recorder()
+    monkeypatch.setattr(schedule, "vc", rec)
+    st = schedule.GroupingState()
+    schedule.run_step(st, "Q", "K", "V", 7, 50, k=8, cold_iters=5, warm_iters=1, stream=object())
+    assert rec.calls[0][:3] == ("cluster", 5, False)
+    assert rec.calls[1] == ("quantize", "pi1", 1)

@@ -34,10 +34,15 @@ _i64 = ctypes.c_int64
 _int = ctypes.c_int
 
 
+# Test aid: the mutation tests point this variable at a build of a copy of
+# vc_oracle.c with one planted mistake, to show that the pins catch it.
+LIB_OVERRIDE_ENV = "VC_ORACLE_LIB_OVERRIDE"
+
+
 def lib():
     global _lib
     if _lib is None:
-        _lib = ctypes.CDLL(_build.build())
+        _lib = ctypes.CDLL(os.environ.get(LIB_OVERRIDE_ENV) or _build.build())
         L = _lib
         L.vco_e4m3_decode.restype = ctypes.c_double
         L.vco_e4m3_decode.argtypes = [ctypes.c_uint8]

@@ -126,6 +126,25 @@ def test_two_dominant_keys_closed_form(oracle_mod, expcast, vsmooth):
                                rtol=1e-12, atol=1e-12)
 
 
+@pytest.mark.parametrize("expcast", [0, 1])
+def test_each_query_block_takes_its_own_scale(oracle_mod, expcast):
+    """sigma_ij = s_q,i s_k,j: rows of query block b see the scores s1 sq_b and
+    s2 sq_b, so alpha_b = 2^(sq_b (s1 - s2)) in the two-key closed form.  The
+    block scales are exact binary fractions; every other key underflows."""
+    N = 700
+    t1, t2, s1, s2 = 5, 3 * 128 + 17, 32.0, 48.0
+    qz = _two_key_case(oracle_mod, s1, s2, t1, t2, N=N, vsmooth=1)
+    sq = np.array([1.0, 0.75, 1.5, 1.25, 0.875, 2.0], np.float32)
+    qz["sq"][0, 0, :] = sq
+    O = oracle_mod.attn(qz, N, softmax_scale=float(LN2), expcast=expcast, vsmooth=1)
+    vq = _dequant_v(oracle_mod, qz, 1)[0, 0]
+    for b, s in enumerate(sq):
+        alpha = 2.0 ** (float(s) * (s1 - s2))
+        want = (alpha * vq[t1] + vq[t2]) / (alpha + 1.0)
+        rows = O[0, 0, 128 * b:min(N, 128 * (b + 1))]
+        np.testing.assert_allclose(rows, np.broadcast_to(want, rows.shape), rtol=1e-12, atol=1e-12)
+
+
 def test_error_bound_against_exact_softmax(oracle_mod):
     """Row max in tile 0 for every row, so every code is relative to the final max."""
     N, d = 640, 64

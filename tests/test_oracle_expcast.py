@@ -49,6 +49,9 @@ def test_clip_range(oracle_mod):
     assert np.all(np.diff(c.astype(int)) >= 0)          # monotone in the score
     # masked / minus-infinity scores give code 0
     assert _direct_codes(oracle_mod, np.array([-np.inf]))[0] == 0
+    # scores above the running max (u > 0) stay at the top code: the clip's upper end
+    hi = _direct_codes(oracle_mod, np.linspace(0.2, 30, 1001))
+    assert np.all(hi == GOLD["clip_hi"]["value"])
 
 
 def test_exact_agreement_per_doubling(oracle_mod):

@@ -2,8 +2,9 @@
 
 [R] 方法步骤详情 step 1: online k-means labels per (batch, head), pi =
 argsort(z).  Pins: every label is a nearest centroid (fp64 brute force), the
-centroids are the means of their members, the objective does not increase,
-the cold start uses tokens floor(i N / k), and pi matches numpy's stable sort.
+centroids are the means of their members (an empty cluster keeps its
+centroid), the objective does not increase, the cold start uses tokens
+floor(i N / k), and pi matches numpy's stable sort.
 """
 import numpy as np
 
@@ -39,6 +40,19 @@ def test_labels_nearest_and_centroids_are_means(oracle_mod):
                     np.testing.assert_allclose(cent[b, h, i], v[b, h][mem].mean(axis=0), rtol=1e-6, atol=1e-6)
                 else:
                     np.testing.assert_array_equal(cent[b, h, i], c_prev[b, h, i])
+
+
+def test_empty_cluster_keeps_its_centroid(oracle_mod):
+    """A centroid no token is nearest to owns no label and is returned unchanged."""
+    V = _v(N=500)
+    k = 6
+    c_prev, _ = oracle_mod.kmeans(V, k, 2)
+    c_prev[:, :, 4] = 1.0e4              # far from every token: cluster 4 stays empty
+    c_prev[0, 1, 2] = -3.0e4             # and cluster 2 of head 1
+    cent, lab = oracle_mod.kmeans(V, k, 1, centroids=c_prev)
+    assert not np.any(lab == 4) and not np.any(lab[0, 1] == 2)
+    np.testing.assert_array_equal(cent[:, :, 4], c_prev[:, :, 4])
+    np.testing.assert_array_equal(cent[0, 1, 2], c_prev[0, 1, 2])
 
 
 def test_cold_start_rule(oracle_mod):

@@ -100,7 +100,8 @@ def test_quantize_strided_input(oracle_mod):
 # 256), k > 256 the fp32 CUDA-core one
 @pytest.mark.parametrize("N,d,H,k,iters", [(1024, 64, 2, 8, 5), (5000, 128, 2, 64, 3), (700, 128, 1, 1, 2),
                                            (4096 * 2 + 77, 128, 1, 37, 2), (2048, 64, 1, 250, 2),
-                                           (4000, 128, 1, 256, 2), (3000, 128, 1, 257, 2), (2000, 64, 1, 1000, 1)])
+                                           (4000, 128, 1, 256, 2), (3000, 128, 1, 257, 2), (2000, 64, 1, 1000, 1),
+                                           (2100, 64, 1, 1024, 1)])
 def test_cluster_invariants(oracle_mod, N, d, H, k, iters):
     Q, K, V = _case(N=N, d=d, H=H, seed=11)
     Vd = V.to(DEV)
@@ -192,6 +193,24 @@ def test_attention_matches_oracle(oracle_mod, case, expcast, vsmooth):
     ref = oracle_mod.attn(qn, N, expcast=expcast, vsmooth=vsmooth)
     got = O.float().cpu().numpy().transpose(0, 2, 1, 3)
     assert _rel(got, ref) <= O_TOL
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("expcast", [1, 0])
+def test_attention_batched_with_scale(oracle_mod, d, expcast):
+    """B = 2 and a softmax scale other than 1/sqrt(d): every (b, h) against the oracle."""
+    N, scale = 700, 0.05
+    Q, K, V = _case(N=N, d=d, H=2, seed=29, B=2)
+    Qd, Kd, Vd = Q.to(DEV), K.to(DEV), V.to(DEV)
+    perm = vc.vc_cluster(Vd, 8, 2)[2]
+    qz = vc.vc_quantize(Qd, Kd, Vd, perm, 1)
+    O = vc.vc_attn_fwd(qz, vc.shape_of(Qd), softmax_scale=scale, expcast=expcast, vsmooth=1)
+    torch.cuda.synchronize()
+    ref = oracle_mod.attn(_gpu_quant_np(qz), N, softmax_scale=scale, expcast=expcast, vsmooth=1)
+    got = O.float().cpu().numpy().transpose(0, 2, 1, 3)
+    for b in range(2):
+        for h in range(2):
+            assert _rel(got[b, h], ref[b, h]) <= O_TOL, (b, h)
 
 
 def test_output_rows_beyond_n_untouched(oracle_mod):

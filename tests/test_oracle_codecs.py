@@ -11,7 +11,6 @@ import math
 import os
 
 import numpy as np
-import pytest
 import torch
 
 GOLD = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "pages_constants.json")))

@@ -14,7 +14,8 @@ activations, which are not available; these stand in for them):
   1% outlier tokens x20 on 4 channels chosen per head; k=64, 5 iterations.
 * ``wan``    B=1 H=40 N=75600 d=128  Q,K ~ N(0,1) + per-(head,channel) bias
   N(0,2); V = 256-centroid mixture, 1% outlier tokens x20 on 4 channels that
-  drift from head to head; k=256, warm-started.
+  change from head to head (each head draws 4 channels, shifted by 3 h);
+  k=256, warm-started.
 * ``sweep``  B=1 H=24 d=128 N in {4096,...,131072}, generated like ``wan``,
   k = N/512.
 

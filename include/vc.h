@@ -143,7 +143,9 @@ vc_status vc_cluster_ex(const void* V, vc_shape shape, int k, int iters, int war
  *
  *   Q, K, V    bf16 [B,N,H,d] with `shape` strides (read only).
  *   perm       int32 [B,H,N] or NULL (identity).  K' = K[perm], V' = V[perm]
- *              (the joint gather); Q keeps its order.
+ *              (the joint gather); Q keeps its order.  Each (b,h) row must be
+ *              a permutation of 0..N-1 (vc_cluster's output is); the entries
+ *              are not checked, and a value outside 0..N-1 is out of contract.
  *   vsmooth    1: subtract each 128-token block mean of V' (kept as bf16 in
  *              `mu`) and quantize the residual; 0: quantize V' directly
  *              (`mu` may be NULL and is not written).
@@ -158,6 +160,12 @@ vc_status vc_cluster_ex(const void* V, vc_shape shape, int k, int iters, int war
  *   workspace  >= vc_quantize_workspace(shape) bytes, 256-byte aligned.
  * Output pointers must be 16-byte aligned.  Codes and scales are
  * deterministic and bit-reproducible.
+ * Errors, all returned before any launch: VC_ERR_INVALID_ARG (a null pointer
+ * -- mu may be NULL only with vsmooth = 0 --, a misaligned Q, K, V, Q8, K8 or
+ * V8T, vsmooth not in {0,1}, a non-positive size, or a stride that is not a
+ * positive multiple of 8), VC_ERR_UNSUPPORTED (d not 64 or 128, N > 2^24, or
+ * B*H*Npad >= 2^31), VC_ERR_WORKSPACE (workspace null, unaligned or too
+ * small); VC_ERR_CUDA if a launch fails.
  */
 size_t vc_quantize_workspace(vc_shape shape);
 vc_status vc_quantize(const void* Q, const void* K, const void* V, vc_shape shape,
@@ -273,7 +281,14 @@ vc_status vc_quantize_static(const void* Q, const void* K, const void* V, vc_sha
  *   softmax_scale  > 0, or <= 0 for 1/sqrt(d).
  *   O        bf16 [B,N,H,d] with `shape` strides (rows in original query order).
  *   dev_status  nullable; receives VC_ERR_TIMEOUT if a device wait ran out.
- * Q8/K8/V8T must be 16-byte aligned (they are read with TMA).
+ * Q8/K8/V8T must be 16-byte aligned (they are read with TMA), and so must O
+ * (rows are written 16 bytes at a time).
+ * Errors, all returned before any launch: VC_ERR_INVALID_ARG (a null pointer
+ * -- mu may be NULL only with vsmooth = 0 --, a misaligned Q8, K8, V8T or O,
+ * expcast or vsmooth not in {0,1}, a non-positive size, or a stride that is
+ * not a positive multiple of 8), VC_ERR_UNSUPPORTED (d not 64 or 128,
+ * N > 2^24, or B*H*Npad >= 2^31); VC_ERR_CUDA if a tensor map cannot be
+ * encoded or the launch fails.
  */
 vc_status vc_attn_fwd(const uint8_t* Q8, const float* sq, const uint8_t* K8, const float* sk,
                       const uint8_t* V8T, const float* sv, const void* mu, vc_shape shape,

@@ -73,6 +73,11 @@ def test_attn_argument_errors(L):
     assert L.vc_attn_fwd(*args, st, 0.0, 1, 1, FAKE, None, None) == 1
     big = _shape(N=(1 << 24) + 1)
     assert L.vc_attn_fwd(*args, big, 0.0, 1, 1, FAKE, None, None) == 2
+    # O is written 16 bytes at a time
+    assert L.vc_attn_fwd(*args, s, 0.0, 1, 1, unaligned, None, None) == 1
+    # B*H*Npad rows must stay below 2^31 (32-bit TMA row coordinates)
+    many = _shape(H=140000, N=16384)
+    assert L.vc_attn_fwd(*args, many, 0.0, 1, 1, FAKE, None, None) == 2
 
 
 def test_quantize_and_cluster_argument_errors(L):
@@ -84,6 +89,8 @@ def test_quantize_and_cluster_argument_errors(L):
     assert L.vc_quantize(*f, s, None, 1, *outs, None, ws_need, None) == 3
     assert L.vc_quantize(*f, s, None, 2, *outs, FAKE, ws_need, None) == 1
     assert L.vc_quantize(*f, s, None, 1, *outs[:6], None, FAKE, ws_need, None) == 1   # mu needed
+    ws_odd = ctypes.c_void_p(0x10000 + 128)   # workspace must be 256-byte aligned
+    assert L.vc_quantize(*f, s, None, 1, *outs, ws_odd, ws_need, None) == 3
     cw = L.vc_cluster_workspace(s, 8)
     assert L.vc_cluster(FAKE, s, 0, 1, 0, FAKE, FAKE, FAKE, FAKE, cw, None, None) == 2
     assert L.vc_cluster(FAKE, s, 2000, 1, 0, FAKE, FAKE, FAKE, FAKE, cw, None, None) == 2

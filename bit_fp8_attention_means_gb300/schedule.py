@@ -10,7 +10,8 @@ Reading used where the pages are silent: a step s clusters when
 s < ceil(0.25 * S) and s % 4 == 0; every other step reuses the last
 permutation.  The first clustering is a cold start (``cold_iters`` Lloyd
 iterations); later ones run ``warm_iters`` iterations from the previous
-centroids.
+centroids.  The centroids and pi are the only state carried between steps;
+``state_dict`` / ``load_state_dict`` checkpoint and restore it.
 """
 import math
 from dataclasses import dataclass, field
@@ -32,6 +33,24 @@ class GroupingState:
     perm: torch.Tensor = None
     workspace: torch.Tensor = None
     clusterings: int = 0
+
+
+def state_dict(state: GroupingState) -> dict:
+    """The cross-step state to checkpoint: centroids, labels, pi and the
+    number of clusterings so far (the workspace is scratch and is not kept)."""
+    return {"centroids": state.centroids, "labels": state.labels, "perm": state.perm,
+            "clusterings": state.clusterings}
+
+
+def load_state_dict(d: dict, device=None) -> GroupingState:
+    """A GroupingState from `state_dict` output, its tensors moved to `device`
+    (as saved when None).  The next clustering warm-starts from the restored
+    centroids and the steps in between reuse the restored pi, as in an
+    uninterrupted run."""
+    def mv(t):
+        return t if t is None or device is None else t.to(device)
+    return GroupingState(centroids=mv(d["centroids"]), labels=mv(d["labels"]), perm=mv(d["perm"]),
+                         clusterings=int(d["clusterings"]))
 
 
 @dataclass

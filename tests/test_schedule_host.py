@@ -8,7 +8,9 @@ centroids, and reuse a permutation for 4 neighbouring steps.  The checks:
 * a step sequence through ``run_step`` with the library calls replaced by a
   recorder: the first clustering is cold, later ones warm from the centroids
   the previous one returned, every other step quantizes with the last pi,
-  ``vsmooth = 0`` never clusters and quantizes with the identity.
+  ``vsmooth = 0`` never clusters and quantizes with the identity;
+* checkpoint and resume: a run saved after any step and restored from the
+  saved bytes makes the same calls as the uninterrupted run.
 """
 import math
 
@@ -90,3 +92,40 @@ def test_missing_permutation_forces_a_clustering(monkeypatch):
     schedule.run_step(st, "Q", "K", "V", 7, 50, k=8, cold_iters=5, warm_iters=1, stream=object())
     assert rec.calls[0][:3] == ("cluster", 5, False)
     assert rec.calls[1] == ("quantize", "pi1", 1)
+
+
+def test_resume_from_checkpoint_matches_uninterrupted(monkeypatch):
+    import io
+
+    import torch
+    S = 50
+    full, _ = _run(monkeypatch, S)
+    for cut in (3, 4, 6, 13):
+        rec = _Recorder()
+        monkeypatch.setattr(schedule, "vc", rec)
+        st = schedule.GroupingState()
+        for s in range(cut):
+            schedule.run_step(st, "Q", "K", "V", s, S, k=8, cold_iters=5, warm_iters=1, stream=object())
+        # the state round-trips through bytes (tensor-valued in real use)
+        st.centroids, st.labels, st.perm = (torch.full((2,), float(st.clusterings)),
+                                            torch.zeros(3, dtype=torch.int32), torch.arange(3, dtype=torch.int32))
+        buf = io.BytesIO()
+        torch.save(schedule.state_dict(st), buf)
+        buf.seek(0)
+        st2 = schedule.load_state_dict(torch.load(buf), device="cpu")
+        assert st2.clusterings == st.clusterings
+        assert torch.equal(st2.centroids, st.centroids) and torch.equal(st2.perm, st.perm)
+        marker = st2.perm
+        ncut = len(rec.calls)
+        for s in range(cut, S):
+            schedule.run_step(st2, "Q", "K", "V", s, S, k=8, cold_iters=5, warm_iters=1, stream=object())
+        kinds = [c[0] for c in rec.calls]
+        assert kinds == [c[0] for c in full.calls]
+        # the first clustering after the resume warm-starts from the restored centroids,
+        # and the steps before it quantize with the restored pi
+        after = rec.calls[ncut:]
+        first = next((i for i, c in enumerate(after) if c[0] == "cluster"), None)
+        if first is not None:
+            assert after[first][1:3] == (1, True) and torch.equal(after[first][3], st.centroids)
+        pre = after[:first] if first is not None else after
+        assert all(c[1] is marker for c in pre if c[0] == "quantize")

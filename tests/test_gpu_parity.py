@@ -82,6 +82,24 @@ def test_quantize_bitexact(oracle_mod, case, vsmooth, use_perm):
         np.testing.assert_array_equal(got["mu"], want["mu"], err_msg="mu")
 
 
+@pytest.mark.parametrize("N,d", [(300, 128), (1000, 64)])
+def test_quantize_poisoned_outputs(oracle_mod, N, d):
+    """Every output buffer pre-filled with 0xFF bytes: the whole of each array,
+    padding rows and columns included, comes out equal to the oracle's."""
+    Q, K, V = _case(N=N, d=d, H=2, seed=31)
+    Qd, Kd, Vd = Q.to(DEV), K.to(DEV), V.to(DEV)
+    out = vc.alloc_quantized(vc.shape_of(Qd), Qd.device, 1)
+    for t in out.values():
+        t.view(torch.uint8).fill_(0xFF)
+    g = torch.Generator().manual_seed(3)
+    perm = torch.stack([torch.randperm(N, generator=g) for _ in range(2)])[None].to(torch.int32)
+    qz = vc.vc_quantize(Qd, Kd, Vd, perm.to(DEV), 1, out=out)
+    got = _gpu_quant_np(qz)
+    want = oracle_mod.quantize(u16(Q), u16(K), u16(V), perm.numpy(), 1)
+    for key in ("Q8", "sq", "K8", "sk", "V8T", "sv", "mu"):
+        np.testing.assert_array_equal(got[key], want[key], err_msg=key)
+
+
 def test_quantize_strided_input(oracle_mod):
     """Q/K/V views into a larger [B, N, H, 3, d] buffer (strided heads)."""
     Q, K, V = _case(N=700, d=128, H=2, seed=7)

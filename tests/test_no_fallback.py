@@ -1,7 +1,8 @@
 """The product path has no CPU fallback (CPU only).
 
 With the CUDA library absent every entry of the binding raises before doing
-any work, and nothing in the package imports the oracle.
+any work; nothing in the package imports the oracle, and the oracle imports
+nothing from the package and includes only system headers.
 """
 import ast
 import glob
@@ -49,3 +50,17 @@ def test_package_never_imports_the_oracle():
             else:
                 continue
             assert not any(n == "oracle" or n.startswith("oracle.") for n in names), (path, names)
+
+
+def test_oracle_shares_no_code_with_the_library():
+    """The oracle imports nothing from the package and includes only system headers."""
+    for path in glob.glob(os.path.join(ROOT, "oracle", "*.py")):
+        tree = ast.parse(open(path).read())
+        for node in ast.walk(tree):
+            if isinstance(node, (ast.Import, ast.ImportFrom)):
+                names = [a.name for a in node.names] if isinstance(node, ast.Import) else [node.module or ""]
+                assert not any(n.startswith("bit_fp8_attention_means_gb300") for n in names), (path, names)
+    for path in glob.glob(os.path.join(ROOT, "oracle", "*.c")):
+        for line in open(path):
+            if line.lstrip().startswith("#include"):
+                assert "<" in line and '"' not in line, (path, line)

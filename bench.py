@@ -1,7 +1,7 @@
 """Benchmark of the VC-Attention hot path on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--mode step|schedule|sweep|preproc]
+                    [--mode step|schedule|sweep|preproc|fill|hybrid]
 
 Default (mode=step): the Wan2.2-shaped workload (B=1, H=40, N=75,600, d=128,
 k=256).  One step = one grouping denoising step of the whole path: warm-started
@@ -12,6 +12,11 @@ metric is FP8 attention TFLOPS, 4 B H N^2 d per step divided by the step time
 Inputs (2.3 GB) are larger than the 129 MB L2, so no flush is needed between
 steps.  Under torchrun every rank runs the full workload on its own GPU (weak
 scaling, no collective on the data path); the time is the max over ranks.
+
+--mode sweep times the attention kernel alone over N = 4,096 ... 131,072
+(H = 24, d = 128) for each of ExpCast / exp-then-cast and V-Smooth on / off.
+--mode schedule runs 50 denoising steps of the Wan2.2 shape with the
+first-quarter, 1-in-4 clustering schedule and reports the clustering share.
 
 --mode preproc times the quantizer with the rotary transform and the Hadamard
 rotation of Q/K fused in (vc_quantize_ex) against the same computation run as

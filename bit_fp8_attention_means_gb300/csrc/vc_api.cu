@@ -1,6 +1,8 @@
 // vc_api.cu -- the extern "C" entry points declared in include/vc.h.
 // Argument checks happen here, on the host, before anything is enqueued.
 #include <cstdint>
+#include <mutex>
+#include <vector>
 
 #include "vc.h"
 #include "vc_internal.h"
@@ -21,6 +23,70 @@ vc_status check_shape(const vc_shape& s) {
 }
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+namespace {
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+
+CtxGetCurrentFn ctx_get_current_fn() {
+    static CtxGetCurrentFn fn = [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            return reinterpret_cast<CtxGetCurrentFn>(ptr);
+        return static_cast<CtxGetCurrentFn>(nullptr);
+    }();
+    return fn;
+}
+
+struct AttrEntry {
+    CtxKey key;
+    const void* kern;
+    int bytes;
+};
+std::mutex g_attr_mutex;
+std::vector<AttrEntry> g_attr_done;
+}  // namespace
+
+vc_status current_ctx(CtxKey* out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return VC_ERR_CUDA;
+    CUcontext ctx = nullptr;
+    CtxGetCurrentFn fn = ctx_get_current_fn();
+    if (fn && fn(&ctx) != CUDA_SUCCESS) ctx = nullptr;
+    out->device = dev;
+    out->ctx = ctx;
+    return VC_OK;
+}
+
+vc_status ensure_smem_attr(const void* kern, int bytes) {
+    CtxKey key;
+    vc_status st = current_ctx(&key);
+    if (st != VC_OK) return st;
+    std::lock_guard<std::mutex> lock(g_attr_mutex);
+    for (const AttrEntry& e : g_attr_done)
+        if (e.kern == kern && e.key == key && e.bytes >= bytes) return VC_OK;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return cuda_status(e);
+    // a context created by this call's own runtime initialisation is known only now
+    if (!key.ctx) current_ctx(&key);
+    g_attr_done.push_back(AttrEntry{key, kern, bytes});
+    return VC_OK;
+}
+
+vc_status quantize_args(const void* Q, const void* K, const void* V, const vc_shape& shape, int vsmooth,
+                        const float* rope, int hadamard, const uint8_t* Q8, const float* sq, const uint8_t* K8,
+                        const float* sk, const uint8_t* V8T, const float* sv, const void* mu) {
+    vc_status st = check_shape(shape);
+    if (st != VC_OK) return st;
+    if ((vsmooth != 0 && vsmooth != 1) || (hadamard != 0 && hadamard != 1)) return VC_ERR_INVALID_ARG;
+    if (!Q || !K || !V || !Q8 || !sq || !K8 || !sk || !V8T || !sv || (vsmooth && !mu)) return VC_ERR_INVALID_ARG;
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(Q8) || !aligned16(K8) || !aligned16(V8T) ||
+        !aligned16(rope))
+        return VC_ERR_INVALID_ARG;
+    return VC_OK;
+}
 
 }  // namespace vc
 
@@ -77,20 +143,6 @@ size_t vc_quantize_workspace(vc_shape shape) {
     return quantize_workspace(shape);
 }
 
-static vc_status quantize_common(const void* Q, const void* K, const void* V, const vc_shape& shape, int vsmooth,
-                                 const float* rope, int hadamard, const uint8_t* Q8, const float* sq,
-                                 const uint8_t* K8, const float* sk, const uint8_t* V8T, const float* sv,
-                                 const void* mu) {
-    vc_status st = check_shape(shape);
-    if (st != VC_OK) return st;
-    if ((vsmooth != 0 && vsmooth != 1) || (hadamard != 0 && hadamard != 1)) return VC_ERR_INVALID_ARG;
-    if (!Q || !K || !V || !Q8 || !sq || !K8 || !sk || !V8T || !sv || (vsmooth && !mu)) return VC_ERR_INVALID_ARG;
-    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(Q8) || !aligned16(K8) || !aligned16(V8T) ||
-        !aligned16(rope))
-        return VC_ERR_INVALID_ARG;
-    return VC_OK;
-}
-
 static bool workspace_ok(const void* ws, size_t bytes, size_t need) {
     return ws && bytes >= need && (reinterpret_cast<uintptr_t>(ws) & 255u) == 0;
 }
@@ -106,7 +158,7 @@ vc_status vc_quantize_ex(const void* Q, const void* K, const void* V, vc_shape s
                          int vsmooth, const float* rope, int hadamard, uint8_t* Q8, float* sq, uint8_t* K8,
                          float* sk, uint8_t* V8T, float* sv, void* mu, void* workspace, size_t workspace_bytes,
                          vc_stream_t stream) {
-    vc_status st = quantize_common(Q, K, V, shape, vsmooth, rope, hadamard, Q8, sq, K8, sk, V8T, sv, mu);
+    vc_status st = quantize_args(Q, K, V, shape, vsmooth, rope, hadamard, Q8, sq, K8, sk, V8T, sv, mu);
     if (st != VC_OK) return st;
     if (!workspace_ok(workspace, workspace_bytes, quantize_workspace(shape))) return VC_ERR_WORKSPACE;
     Preproc pp;
@@ -126,7 +178,7 @@ vc_status vc_quantize_staged(const void* Q, const void* K, const void* V, vc_sha
                              int vsmooth, const float* rope, int hadamard, uint8_t* Q8, float* sq, uint8_t* K8,
                              float* sk, uint8_t* V8T, float* sv, void* mu, void* workspace, size_t workspace_bytes,
                              vc_stream_t stream) {
-    vc_status st = quantize_common(Q, K, V, shape, vsmooth, rope, hadamard, Q8, sq, K8, sk, V8T, sv, mu);
+    vc_status st = quantize_args(Q, K, V, shape, vsmooth, rope, hadamard, Q8, sq, K8, sk, V8T, sv, mu);
     if (st != VC_OK) return st;
     if (!workspace_ok(workspace, workspace_bytes, quantize_staged_workspace(shape))) return VC_ERR_WORKSPACE;
     Preproc pp;
@@ -189,6 +241,22 @@ vc_status vc_attn_fwd_debug(const uint8_t* Q8, const float* sq, const uint8_t* K
     return launch_attn(Q8, sq, K8, sk, V8T, sv, static_cast<const uint16_t*>(mu), shape, softmax_scale, expcast,
                        exact_margin, vsmooth, static_cast<uint16_t*>(O), dev_status,
                        reinterpret_cast<cudaStream_t>(stream), &dbg);
+}
+
+vc_status vc_debug_attn_timeout(const uint8_t* Q8, const float* sq, const uint8_t* K8, const float* sk,
+                                const uint8_t* V8T, const float* sv, const void* mu, vc_shape shape, int vsmooth,
+                                void* O, int32_t* dev_status, vc_stream_t stream, int skip_k_tile,
+                                uint32_t timeout_us) {
+    vc_status st = attn_common(Q8, sq, K8, sk, V8T, sv, mu, shape, 1, vsmooth, O);
+    if (st != VC_OK) return st;
+    if (!dev_status || skip_k_tile < 0 || skip_k_tile >= nblk_of(shape.N) || timeout_us == 0 ||
+        timeout_us > 10000000u)
+        return VC_ERR_INVALID_ARG;
+    AttnDebug dbg;
+    dbg.skip_k_tile = skip_k_tile;
+    dbg.timeout_ns = (uint64_t)timeout_us * 1000ull;
+    return launch_attn(Q8, sq, K8, sk, V8T, sv, static_cast<const uint16_t*>(mu), shape, 0.f, 1, 0.f, vsmooth,
+                       static_cast<uint16_t*>(O), dev_status, reinterpret_cast<cudaStream_t>(stream), &dbg);
 }
 
 }  // extern "C"

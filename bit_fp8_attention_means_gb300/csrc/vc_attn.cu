@@ -48,7 +48,7 @@
 // ExpCast inner loop, per score: ts = sat(acc * sigma/16 + C/128) (one FFMA
 // with saturation = clip to [0, 128] of t/128, exact because /128 and /16 are
 // powers of two), then b = ts*128 + 1.5*2^23 (packed FFMA2) whose low byte is
-// rint(t); two integer multiply-adds and one byte permute pack four codes.
+// rint(t); three byte permutes pack four codes.
 // The upper clip at 120 is implied while |m'| < 2^19 (t <= 119.65 + 2^-1);
 // warps with a row beyond take a path with an explicit min.
 #include <cstdio>
@@ -135,6 +135,7 @@ struct AttnParams {
     float exact_margin;  // hybrid: a tile is exact if some row's tile max is within this of its running max (log2)
     int32_t* dev_status;
     uint64_t timeout_ns;
+    int skip_k_tile;     // test hook: the K loader never loads (nor signals) this key tile; -1 = off
     int dbg_bh, dbg_qtile;
     float* S_dump;
     uint8_t* P_dump;
@@ -169,8 +170,9 @@ __device__ __forceinline__ uint32_t expcast4(const float* a, float k1, float k2)
         u2 = min(u2 & 0xFFu, 120u);
         u3 = min(u3 & 0xFFu, 120u);
     }
-    // low 16 bits of u0 + 256 u1 are c0 | c1 << 8 (the magic's low 16 bits are 0)
-    return prmt(mad_lo(u1, 256u, u0), mad_lo(u3, 256u, u2), 0x5410u);
+    // byte permutes gather the four low bytes (c0 | c1 << 8, c2 | c3 << 8, then
+    // both halves), keeping the packing off the FMA pipes
+    return prmt(prmt(u0, u1, 0x0040u), prmt(u2, u3, 0x0040u), 0x5410u);
 }
 
 __device__ __forceinline__ uint16_t bf16_rn_bits(float x) { return __bfloat16_as_ushort(__float2bfloat16_rn(x)); }
@@ -299,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int s = j % NSK;
             if (j >= NSK && !mbar_wait_warp(bar(C::B_KE + s), (j / NSK - 1) & 1, abort_flag, p.dev_status, tmo))
                 break;
-            if (lane == 0) {
+            if (lane == 0 && j != p.skip_k_tile) {
                 mbar_expect_tx(bar(C::B_KF + s), C::KB);
                 tma_load_2d(sbase + C::OFF_K + s * C::KB, &tmK, 0, row0 + j * 128, bar(C::B_KF + s));
                 mbar_arrive(bar(C::B_KF + s));
@@ -308,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // let this CTA's own copies in flight land before the CTA can exit
         for (int j = (issued > NSK ? issued - NSK : 0); j < issued; ++j)
-            drain_wait(bar(C::B_KF + j % NSK), (j / NSK) & 1, tmo);
+            if (j != p.skip_k_tile) drain_wait(bar(C::B_KF + j % NSK), (j / NSK) & 1, tmo);
         drain_wait(bar(C::B_Q), 0, tmo);
     } else if (warp == kVLoadWarp) {
         // ------------------------------------------------------------ V loader
@@ -771,12 +773,8 @@ template <int D, int E, bool S, bool G>
 vc_status launch_one(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const AttnParams& p,
                      dim3 grid, cudaStream_t st) {
     auto kern = attn_fwd_kernel<D, E, S, G>;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::SMEM);
-        if (e != cudaSuccess) return cuda_status(e);
-        attr = true;
-    }
+    vc_status a = ensure_smem_attr(reinterpret_cast<const void*>(kern), Cfg<D>::SMEM);
+    if (a != VC_OK) return a;
     kern<<<grid, kThreads, Cfg<D>::SMEM, st>>>(mq, mk, mv, p);
     return cuda_status(cudaGetLastError());
 }
@@ -849,14 +847,16 @@ vc_status launch_attn(const uint8_t* Q8, const float* sq, const uint8_t* K8, con
     p.kscale = (float)(sc * 1.4426950408889634);
     p.exact_margin = exact_margin;
     p.dev_status = dev_status;
-    p.timeout_ns = 4000000000ull;
-    p.dbg_bh = dbg ? dbg->bh : -1;
-    p.dbg_qtile = dbg ? dbg->qtile : -1;
-    p.S_dump = dbg ? dbg->S : nullptr;
-    p.P_dump = dbg ? dbg->P : nullptr;
+    p.timeout_ns = (dbg && dbg->timeout_ns) ? dbg->timeout_ns : 4000000000ull;
+    p.skip_k_tile = dbg ? dbg->skip_k_tile : -1;
+    const bool dumps = dbg && dbg->S;
+    p.dbg_bh = dumps ? dbg->bh : -1;
+    p.dbg_qtile = dumps ? dbg->qtile : -1;
+    p.S_dump = dumps ? dbg->S : nullptr;
+    p.P_dump = dumps ? dbg->P : nullptr;
     const dim3 grid((nblk + 1) / 2, s.H, s.B);  // two query tiles per CTA
-    if (s.d == 128) return launch_d<128>(mq, mk, mv, p, grid, st, expcast, vsmooth, dbg != nullptr);
-    return launch_d<64>(mq, mk, mv, p, grid, st, expcast, vsmooth, dbg != nullptr);
+    if (s.d == 128) return launch_d<128>(mq, mk, mv, p, grid, st, expcast, vsmooth, dumps);
+    return launch_d<64>(mq, mk, mv, p, grid, st, expcast, vsmooth, dumps);
 }
 
 }  // namespace vc

@@ -777,13 +777,12 @@ static vc_status launch_cluster_d(const uint16_t* V, const vc_shape& s, int k, i
     ClusterWs w = carve(ws, s, k);
     if (!warm) init_centroids<<<dim3(k, BH), 128, 0, st>>>(V, s, k, cent);
     const size_t assign_smem = (size_t)D * (kTokTile + 4) * 4 + (size_t)D * (kCenTile + 4) * 4;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaFuncSetAttribute(assign_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)assign_smem);
-        cudaFuncSetAttribute(assign_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, AsCfg<D>::SMEM);
-        attr_set = true;
-    }
     const bool tc = k <= kAsMaxK;
+    {
+        vc_status a = tc ? ensure_smem_attr(reinterpret_cast<const void*>(assign_tc_kernel<D>), AsCfg<D>::SMEM)
+                         : ensure_smem_attr(reinterpret_cast<const void*>(assign_kernel<D>), (int)assign_smem);
+        if (a != VC_OK) return a;
+    }
     CUtensorMap vmap;
     int grid_tc = 0;
     const int tiles_per_head = (s.N + 127) / 128;
@@ -816,12 +815,8 @@ static vc_status launch_cluster_d(const uint16_t* V, const vc_shape& s, int k, i
         const size_t fbase = ((size_t)4 * k * sizeof(int32_t) + k + 15) & ~size_t(15);
         const size_t tbytes = (size_t)k * D * sizeof(float);
         if (fbase + tbytes <= kFillSmemT) {
-            static bool fattr = false;
-            if (!fattr) {
-                cudaFuncSetAttribute(fill_chain_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)kFillSmemT);
-                fattr = true;
-            }
+            vc_status a = ensure_smem_attr(reinterpret_cast<const void*>(fill_chain_kernel<D, true>), (int)kFillSmemT);
+            if (a != VC_OK) return a;
             fill_chain_kernel<D, true><<<BH, kFillThreads, fbase + tbytes, st>>>(w.count, cent, k, w.cT, w.fdst,
                                                                                  w.ldst);
         } else {

@@ -16,6 +16,27 @@ inline int64_t npad_of(int N) { return (int64_t)nblk_of(N) * kBlock; }
 vc_status check_shape(const vc_shape& s);
 vc_status cuda_status(cudaError_t e);
 
+// The CUDA context current on this host thread and its device: the key of
+// every per-device cache below (a context destroyed by a device reset and
+// recreated gets a new handle, so nothing cached for the old one is reused).
+struct CtxKey {
+    int device = -1;
+    const void* ctx = nullptr;
+    bool operator==(const CtxKey& o) const { return device == o.device && ctx == o.ctx; }
+};
+vc_status current_ctx(CtxKey* out);
+
+// Raises the dynamic shared-memory limit of kernel `kern` to `bytes` once per
+// context (cudaFuncSetAttribute acts on the current context only).  Thread
+// safe: host threads may launch on one or several devices concurrently.
+vc_status ensure_smem_attr(const void* kern, int bytes);
+
+// Argument checks shared by the quantizer entry points (vc_quantize,
+// vc_quantize_ex, vc_quantize_staged, vc_quantize_static).
+vc_status quantize_args(const void* Q, const void* K, const void* V, const vc_shape& shape, int vsmooth,
+                        const float* rope, int hadamard, const uint8_t* Q8, const float* sq, const uint8_t* K8,
+                        const float* sk, const uint8_t* V8T, const float* sv, const void* mu);
+
 // cuTensorMapEncodeTiled, looked up through the runtime so that the library
 // does not link against the driver library directly; null if unavailable.
 PFN_cuTensorMapEncodeTiled_v12000 encode_tiled_fn();
@@ -42,9 +63,11 @@ vc_status launch_cluster(const uint16_t* V, const vc_shape& s, int k, int iters,
 
 // attention (vc_attn.cu)
 struct AttnDebug {
-    int bh = -1, qtile = -1;
+    int bh = -1, qtile = -1;       // the query tile whose scores and bytes are dumped (with S, P)
     float* S = nullptr;
     uint8_t* P = nullptr;
+    int skip_k_tile = -1;          // >= 0: the K loader never loads nor signals this key tile
+    uint64_t timeout_ns = 0;       // bound of every device wait (0: the default, 4 s)
 };
 vc_status launch_attn(const uint8_t* Q8, const float* sq, const uint8_t* K8, const float* sk, const uint8_t* V8T,
                       const float* sv, const uint16_t* mu, const vc_shape& s, float softmax_scale, int expcast,

@@ -682,9 +682,8 @@ static cudaError_t launch_qk(const QkArgs& qa, const QkArgs& ka, const vc_shape&
 template <int D, bool ROPE, bool HAD>
 static cudaError_t launch_qk_pre(const QkArgs& qa, const QkArgs& ka, const vc_shape& s, cudaStream_t st) {
     constexpr int smem = PreCfg<D, ROPE>::SMEM;
-    cudaError_t e = cudaFuncSetAttribute(quant_qk_pre_kernel<D, ROPE, HAD>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
+    if (ensure_smem_attr(reinterpret_cast<const void*>(quant_qk_pre_kernel<D, ROPE, HAD>), smem) != VC_OK)
+        return cudaErrorInvalidValue;
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -810,26 +809,41 @@ namespace {
 constexpr size_t kStaticScratchWords = 65536;  // B*H*d <= 65536 (256 KB, held by every GPU that loads the library)
 __device__ __align__(256) uint32_t g_quantize_scratch[kStaticScratchWords];
 
-constexpr int kMaxDevices = 64;
+constexpr int kMaxContexts = 64;
 std::mutex g_scratch_mutex;
-void* g_scratch_addr[kMaxDevices] = {};
+struct ScratchEntry {
+    CtxKey key;
+    void* addr;
+};
+ScratchEntry g_scratch_addr[kMaxContexts] = {};
+int g_scratch_n = 0;
 
-// Device address of g_quantize_scratch on the current device; looked up once
-// per device (the host-side name is only a stand-in, never a device pointer).
+// Device address of g_quantize_scratch in the current context; looked up once
+// per context, with that context's device current (the host-side name is only
+// a stand-in, never a device pointer).  Keyed by the context handle, so a
+// context destroyed by a device reset and recreated gets a fresh lookup.
 vc_status static_scratch(void** out) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return VC_ERR_CUDA;
+    CtxKey key;
+    if (current_ctx(&key) != VC_OK) return VC_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (!g_scratch_addr[dev]) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_quantize_scratch) != cudaSuccess || !p) return VC_ERR_CUDA;
-        g_scratch_addr[dev] = p;
+    if (key.ctx) {
+        for (int i = 0; i < g_scratch_n; ++i)
+            if (g_scratch_addr[i].key == key) {
+                *out = g_scratch_addr[i].addr;
+                return VC_OK;
+            }
     }
-    *out = g_scratch_addr[dev];
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_quantize_scratch) != cudaSuccess || !p) return VC_ERR_CUDA;
+    // the lookup initialises the context if none was current yet
+    if (!key.ctx && current_ctx(&key) != VC_OK) return VC_ERR_CUDA;
+    if (key.ctx) {
+        if (g_scratch_n < kMaxContexts) g_scratch_addr[g_scratch_n++] = ScratchEntry{key, p};
+        else g_scratch_addr[kMaxContexts - 1] = ScratchEntry{key, p};
+    }
+    *out = p;
     return VC_OK;
 }
-
-bool aligned16_q(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
 }  // namespace vc
@@ -838,13 +852,8 @@ extern "C" vc_status vc_quantize_static(const void* Q, const void* K, const void
                                         const int32_t* perm, int vsmooth, uint8_t* Q8, float* sq, uint8_t* K8,
                                         float* sk, uint8_t* V8T, float* sv, void* mu, vc_stream_t stream) {
     using namespace vc;
-    vc_status st = check_shape(shape);
+    vc_status st = quantize_args(Q, K, V, shape, vsmooth, nullptr, 0, Q8, sq, K8, sk, V8T, sv, mu);
     if (st != VC_OK) return st;
-    if (vsmooth != 0 && vsmooth != 1) return VC_ERR_INVALID_ARG;
-    if (!Q || !K || !V || !Q8 || !sq || !K8 || !sk || !V8T || !sv || (vsmooth && !mu)) return VC_ERR_INVALID_ARG;
-    if (!aligned16_q(Q) || !aligned16_q(K) || !aligned16_q(V) || !aligned16_q(Q8) || !aligned16_q(K8) ||
-        !aligned16_q(V8T))
-        return VC_ERR_INVALID_ARG;
     if ((size_t)shape.B * shape.H * shape.d > kStaticScratchWords) return VC_ERR_WORKSPACE;
     void* scratch = nullptr;
     st = static_scratch(&scratch);

@@ -36,9 +36,13 @@ class GroupingState:
 
 
 def state_dict(state: GroupingState) -> dict:
-    """The cross-step state to checkpoint: centroids, labels, pi and the
-    number of clusterings so far (the workspace is scratch and is not kept)."""
-    return {"centroids": state.centroids, "labels": state.labels, "perm": state.perm,
+    """The cross-step state to checkpoint: copies of the centroids, labels and
+    pi, and the number of clusterings so far (the workspace is scratch and is
+    not kept).  Copies, because later clustering steps write the live tensors
+    in place: a checkpoint held in memory stays what it was when taken."""
+    def cp(t):
+        return None if t is None else t.clone()
+    return {"centroids": cp(state.centroids), "labels": cp(state.labels), "perm": cp(state.perm),
             "clusterings": state.clusterings}
 
 

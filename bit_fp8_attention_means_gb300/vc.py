@@ -76,6 +76,9 @@ def lib():
         L.vc_debug_e4m3_encode.argtypes = [_vp, ctypes.c_int64, _vp, _vp]
         L.vc_debug_wait_timeout.restype = ctypes.c_int
         L.vc_debug_wait_timeout.argtypes = [_vp, ctypes.c_uint32, _vp]
+        L.vc_debug_attn_timeout.restype = ctypes.c_int
+        L.vc_debug_attn_timeout.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, VcShape, ctypes.c_int, _vp, _vp, _vp,
+                                            ctypes.c_int, ctypes.c_uint32]
         _lib = L
     return _lib
 
@@ -281,3 +284,17 @@ def vc_debug_e4m3_encode(x: torch.Tensor, out=None, stream=None):
 
 def vc_debug_wait_timeout(dev_status: torch.Tensor, timeout_us: int, stream=None):
     _check(lib().vc_debug_wait_timeout(_ptr(dev_status), int(timeout_us), _stream(stream)), "vc_debug_wait_timeout")
+
+
+def vc_debug_attn_timeout(qz, shape: VcShape, dev_status: torch.Tensor, skip_k_tile: int, timeout_us: int,
+                          vsmooth=1, O=None, stream=None):
+    """vc_attn_fwd whose K loader never delivers key tile `skip_k_tile`, every
+    device wait bounded by timeout_us: the kernel must record VC_ERR_TIMEOUT in
+    dev_status and return.  Returns O (unspecified contents)."""
+    if O is None:
+        O = torch.empty((shape.B, shape.N, shape.H, shape.d), dtype=torch.bfloat16, device=qz["Q8"].device)
+    _check(lib().vc_debug_attn_timeout(_ptr(qz["Q8"]), _ptr(qz["sq"]), _ptr(qz["K8"]), _ptr(qz["sk"]),
+                                       _ptr(qz["V8T"]), _ptr(qz["sv"]), _ptr(qz["mu"]) if vsmooth else None, shape,
+                                       int(vsmooth), _ptr(O), _ptr(dev_status), _stream(stream), int(skip_k_tile),
+                                       int(timeout_us)), "vc_debug_attn_timeout")
+    return O

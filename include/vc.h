@@ -21,7 +21,9 @@
  * Conventions shared by every entry point
  *   - Every pointer is device memory owned by the caller unless stated.  The
  *     library never allocates or frees memory and keeps no per-call state;
- *     calls on different streams with disjoint buffers may run concurrently.
+ *     calls on different streams with disjoint buffers may run concurrently,
+ *     from one or several host threads and on one or several devices (the
+ *     one-time launch set-up is done per CUDA context, under a lock).
  *   - All work is enqueued asynchronously on `stream` (NULL = legacy default
  *     stream).  A return of VC_OK means the launches were enqueued.
  *   - Argument and shape errors are detected on the host before anything is
@@ -249,9 +251,10 @@ vc_status vc_quantize_staged(const void* Q, const void* K, const void* V, vc_sha
  * VC_ERR_WORKSPACE without launching.  Nothing is allocated: no cudaMalloc,
  * no cudaFree, no allocating library routine.
  *
- * The first call on each device looks up the array's device address (with
- * that device current) and caches it; make that first call before any stream
- * capture begins.  Every call shares the one array and clears what it needs
+ * The first call in each CUDA context (normally one per device: the primary
+ * context) looks up the array's device address, with that context current,
+ * and caches it; make that first call before any stream capture begins.
+ * After a device reset the next call looks it up again.  Every call shares the one array and clears what it needs
  * at its start, so calls whose work overlaps on the GPU (different streams,
  * or different host threads on one device) race and must be serialized by
  * the caller.
@@ -348,6 +351,22 @@ vc_status vc_debug_e4m3_encode(const float* x, int64_t n, uint8_t* out, vc_strea
  * and the kernel returns; the CUDA context stays usable.
  */
 vc_status vc_debug_wait_timeout(int32_t* dev_status, uint32_t timeout_us, vc_stream_t stream);
+
+/*
+ * Test hook for the attention kernel's own failure path: runs vc_attn_fwd
+ * (expcast = 1) except that its K loader never loads, nor signals, key tile
+ * `skip_k_tile` (0 <= skip_k_tile < nblk), and every device wait is bounded
+ * by timeout_us microseconds (1 .. 10^7) instead of 4 s.  The wait for that
+ * tile runs out: the kernel writes VC_ERR_TIMEOUT to *dev_status (required
+ * here), every warp of the CTA stops waiting, the CTA's own copies and MMAs
+ * in flight drain, its tensor memory is freed and the kernel returns; O is
+ * left unspecified.  The CUDA context stays usable.  Same other arguments as
+ * vc_attn_fwd.
+ */
+vc_status vc_debug_attn_timeout(const uint8_t* Q8, const float* sq, const uint8_t* K8, const float* sk,
+                                const uint8_t* V8T, const float* sv, const void* mu, vc_shape shape,
+                                int vsmooth, void* O, int32_t* dev_status, vc_stream_t stream,
+                                int skip_k_tile, uint32_t timeout_us);
 
 #ifdef __cplusplus
 }

@@ -283,3 +283,64 @@ def attn_ref(Q, K, V, softmax_scale: float = 0.0, rows=None) -> np.ndarray:
     O = np.zeros((B, H, rows.size, d), np.float64)
     assert lib().vco_attn_ref(Q, K, V, B, H, N, d, sb, sn, sh, float(scale), rows, rows.size, O) == 0
     return O
+
+
+# ---------------------------------------------------------------- O comparison
+
+# Bars for comparing a bf16 attention output with this oracle's fp64 output on
+# the same quantized inputs (see check_o).
+O_TOL = 2e-3                 # relative L2 over the whole compared tensor
+O_ROW_TOL = 2.0 ** -8 + 5e-4  # relative L2 of every query row
+O_ELEM_REL = 2.0 ** -8       # per element: bf16 rounding of the kernel's value ...
+O_ELEM_ROWRMS = 2e-3         # ... plus this fraction of the row's RMS
+O_ELEM_ROWRMS_EXP = 2e-2     # ... or this one where the bytes come from an exponential (see check_o)
+O_ROW_TOL_EXP = 1e-2         # row bar where the bytes come from an exponential
+
+
+def check_o(got, ref, where="", exp_bytes=False):
+    """Compare a kernel output with the oracle, element by element.
+
+    got, ref: arrays [..., rows, d] (got the kernel's bf16 values as floats,
+    ref this oracle's fp64 output for the same rows).  Three bars, each
+    derived from what separates the two:
+      * bf16 rounding of the kernel's output: half an ulp is at most 2^-8 of
+        the element, so no element can differ by more than 2^-8 |ref| for
+        that reason, and no row's relative L2 by more than 2^-8;
+      * the kernel's arithmetic (fp32 tensor-core sums in another order, the
+        rescale factor from a hardware exp2, the mean term through bf16
+        hi/lo parts) moves O by ~1e-4 of the row's RMS, well inside
+        O_ELEM_ROWRMS = 2e-3 and the 5e-4 added to the row bar.
+    Bars: the whole tensor within O_TOL (2e-3) relative L2; every query row
+    within O_ROW_TOL; every element within O_ELEM_REL |ref| + O_ELEM_ROWRMS
+    rms(ref row).  A row that is wrong by a few percent passes the first bar
+    but fails the other two.  Returns the worst ratios (observed / bar).
+
+    exp_bytes: the compared output took some probability bytes from an
+    exponential (exp-then-cast, or the exact tiles of the hybrid bytes).  The
+    kernel's hardware exp2 is not correctly rounded, so up to about one byte
+    in 10^3 lands one E4M3 step away from the oracle's; one step moves that
+    probability by at most 1/8 of itself, and a heavy key moved so shifts
+    its row by up to ~1/8 of its weight times its distance from the row's
+    output -- a few 1e-3 of the row on the test workloads, whose largest
+    single-key weights are a few percent.  The row bar is then
+    O_ROW_TOL_EXP (1e-2) and the per-element allowance O_ELEM_ROWRMS_EXP
+    (2e-2) of the row's RMS; the tensor bar stays 2e-3, and a row wrong by a
+    few percent still fails.
+    """
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    diff = got - ref
+    tot = float(np.linalg.norm(diff) / max(np.linalg.norm(ref), 1e-300))
+    rnorm = np.linalg.norm(ref, axis=-1)
+    rrel = np.linalg.norm(diff, axis=-1) / np.maximum(rnorm, 1e-300)
+    rms = (rnorm / math.sqrt(ref.shape[-1]))[..., None]
+    bound = O_ELEM_REL * np.abs(ref) + (O_ELEM_ROWRMS_EXP if exp_bytes else O_ELEM_ROWRMS) * rms
+    row_tol = O_ROW_TOL_EXP if exp_bytes else O_ROW_TOL
+    eratio = np.abs(diff) / np.maximum(bound, 1e-300)
+    stats = {"total": tot / O_TOL, "row": float(rrel.max()) / row_tol, "elem": float(eratio.max())}
+    msg = "%s: rel-L2 %.3e (bar %.1e), worst row %.3e at %s (bar %.2e), worst element %.2f x its bar at %s" % (
+        where, tot, O_TOL, float(rrel.max()), np.unravel_index(int(np.argmax(rrel)), rrel.shape), row_tol,
+        float(eratio.max()), np.unravel_index(int(np.argmax(eratio)), eratio.shape))
+    assert tot <= O_TOL and float(rrel.max()) <= row_tol and float(eratio.max()) <= 1.0, msg
+    return stats

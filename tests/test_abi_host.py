@@ -101,6 +101,12 @@ def test_quantize_and_cluster_argument_errors(L):
     small = _shape(N=4)
     assert L.vc_cluster(FAKE, small, 8, 1, 0, FAKE, FAKE, FAKE, FAKE, 1 << 20, None, None) == 1
     assert L.vc_debug_wait_timeout(None, 10, None) == 1
+    s3 = _shape(N=300)   # 3 key tiles
+    args = [FAKE] * 7
+    assert L.vc_debug_attn_timeout(*args, s3, 1, FAKE, None, None, 1, 1000) == 1     # dev_status required
+    assert L.vc_debug_attn_timeout(*args, s3, 1, FAKE, FAKE, None, 3, 1000) == 1     # tile out of range
+    assert L.vc_debug_attn_timeout(*args, s3, 1, FAKE, FAKE, None, 0, 0) == 1        # zero bound
+    assert L.vc_debug_attn_timeout(*args, _shape(d=96), 1, FAKE, FAKE, None, 0, 10) == 2
     assert L.vc_cluster_ex(FAKE, s, 8, 1, 0, 2, FAKE, FAKE, FAKE, FAKE, cw, None, None) == 1   # block_fill flag
     assert L.vc_cluster_ex(FAKE, s, 8, 1, 0, 1, FAKE, FAKE, FAKE, FAKE, cw - 1, None, None) == 3
 

@@ -64,3 +64,18 @@ def test_measured_peaks_read_from_file():
         assert p["source"] == "measured" and p["hbm_gbs"] == d["hbm_gbs"] and p["bf16_tflops"] == d["bf16_tflops"]
     else:
         assert p["source"] == "fallback" and p["hbm_gbs"] == 6800.0
+
+
+def test_fp8_peak_burst_only_at_full_clock_without_power_cap():
+    peaks = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "sustained_sm_mhz": 1450.0}
+    full = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": []}
+    p = bench.fp8_peak_for(peaks, full)
+    assert p["which"] == "burst" and p["peak"] == 3800.0 and p["sustained"] == 3400.0
+    assert p["clock_matched"] == pytest.approx(3400.0 * 2070.0 / 1450.0)
+    capped = dict(full, reasons=["sw_power_cap"])
+    assert bench.fp8_peak_for(peaks, capped)["which"] == "sustained"
+    slow = dict(full, sm_mhz=1800.0)
+    assert bench.fp8_peak_for(peaks, slow)["peak"] == 3400.0
+    none = {"sm_mhz": None, "sm_max_mhz": None, "reasons": []}
+    p = bench.fp8_peak_for(dict(peaks, sustained_sm_mhz=None), none)
+    assert p["which"] == "sustained" and p["clock_matched"] is None

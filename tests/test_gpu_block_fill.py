@@ -56,7 +56,7 @@ def test_attention_on_block_fill(oracle_mod):
         np.testing.assert_array_equal(qz[key].cpu().numpy(), want[key], err_msg=key)
     ref = oracle_mod.attn(want, 2000)
     got = O.float().cpu().numpy().transpose(0, 2, 1, 3)
-    assert np.linalg.norm(got - ref) / np.linalg.norm(ref) <= 2e-3
+    oracle_mod.check_o(got, ref, "block fill")
 
 
 def test_block_fill_batched_warm(oracle_mod):

@@ -129,3 +129,35 @@ def test_resume_from_checkpoint_matches_uninterrupted(monkeypatch):
             assert after[first][1:3] == (1, True) and torch.equal(after[first][3], st.centroids)
         pre = after[:first] if first is not None else after
         assert all(c[1] is marker for c in pre if c[0] == "quantize")
+
+
+def test_in_memory_checkpoint_is_not_changed_by_later_steps(monkeypatch):
+    """A checkpoint kept in memory (not serialized) is a copy: a later
+    clustering that writes the live tensors in place leaves it as taken, and a
+    resume from it matches the state at the cut."""
+    import torch
+
+    class InPlace(_Recorder):
+        def vc_cluster(self, V, k, iters, warm_start=False, centroids=None, labels=None, perm=None,
+                       workspace=None, stream=None):
+            self.n += 1
+            self.calls.append(("cluster", iters, warm_start, centroids))
+            if centroids is None:
+                return torch.zeros(4), torch.zeros(3, dtype=torch.int32), torch.arange(3, dtype=torch.int32)
+            centroids.add_(1.0)        # the device call updates its arguments in place
+            labels.add_(1)
+            perm.copy_(perm.flip(0))
+            return centroids, labels, perm
+
+    rec = InPlace()
+    monkeypatch.setattr(schedule, "vc", rec)
+    st = schedule.GroupingState()
+    schedule.run_step(st, "Q", "K", "V", 0, 50, k=8, cold_iters=5, warm_iters=1, stream=object())
+    ck = schedule.state_dict(st)
+    at_cut = (st.centroids.clone(), st.labels.clone(), st.perm.clone())
+    schedule.run_step(st, "Q", "K", "V", 4, 50, k=8, cold_iters=5, warm_iters=1, stream=object())
+    assert not torch.equal(st.centroids, at_cut[0])          # the live state moved on
+    for got, want in zip((ck["centroids"], ck["labels"], ck["perm"]), at_cut):
+        assert torch.equal(got, want)
+    st2 = schedule.load_state_dict(ck)
+    assert torch.equal(st2.centroids, at_cut[0]) and torch.equal(st2.perm, at_cut[2]) and st2.clusterings == 1

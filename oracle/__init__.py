@@ -67,6 +67,15 @@ def lib():
         L.vco_quantize.argtypes = [_u16p, _u16p, _u16p, _int, _int, _int, _int, _i64, _i64, _i64,
                                    ctypes.c_void_p, _int, _u8p, _f32p, _u8p, _f32p, _u8p, _f32p,
                                    ctypes.c_void_p]
+        L.vco_e2m1_decode.restype = ctypes.c_double
+        L.vco_e2m1_decode.argtypes = [ctypes.c_uint8]
+        L.vco_e2m1_encode.restype = ctypes.c_uint8
+        L.vco_e2m1_encode.argtypes = [ctypes.c_float]
+        L.vco_e2m1_encode_arr.argtypes = [_f32p, _i64, _u8p]
+        L.vco_quantize_v4.restype = _int
+        L.vco_quantize_v4.argtypes = [_u16p, _u16p, _u16p, _int, _int, _int, _int, _i64, _i64, _i64,
+                                      ctypes.c_void_p, _int, _u8p, _f32p, _u8p, _f32p, _u8p, _f32p,
+                                      ctypes.c_void_p]
         L.vco_quantize_ex.restype = _int
         L.vco_quantize_ex.argtypes = [_u16p, _u16p, _u16p, _int, _int, _int, _int, _i64, _i64, _i64,
                                       ctypes.c_void_p, _int, ctypes.c_void_p, _int,
@@ -109,6 +118,17 @@ def e4m3_encode(x) -> np.ndarray:
     a = np.ascontiguousarray(x, dtype=np.float32).ravel()
     out = np.empty(a.size, np.uint8)
     lib().vco_e4m3_encode_arr(a, a.size, out)
+    return out.reshape(np.shape(x))
+
+
+def e2m1_decode(code) -> float:
+    return lib().vco_e2m1_decode(int(code))
+
+
+def e2m1_encode(x) -> np.ndarray:
+    a = np.ascontiguousarray(x, dtype=np.float32).ravel()
+    out = np.empty(a.size, np.uint8)
+    lib().vco_e2m1_encode_arr(a, a.size, out)
     return out.reshape(np.shape(x))
 
 
@@ -209,10 +229,12 @@ def block_fill(labels, centroids) -> np.ndarray:
     return perm
 
 
-def quantize(Q, K, V, perm=None, vsmooth: int = 1, rope=None, hadamard: int = 0):
+def quantize(Q, K, V, perm=None, vsmooth: int = 1, rope=None, hadamard: int = 0, vbits: int = 8):
     """Q/K/V quantizer.  With ``rope`` (fp32 [N, d/2, 2]) and/or ``hadamard``
     the Q and K rows are rotated / Hadamard-transformed before quantization
-    and sq carries the factor 1/d."""
+    and sq carries the factor 1/d.  vbits = 4 keeps the V residual in the 4-bit
+    form (E2M1 with a power-of-two scale per 32 tokens of a channel, stored as
+    the equal E4M3 byte; sv = amax/6); it takes no rotary table or Hadamard."""
     Q, (sb, sn, sh) = _bnhd(Q)
     K, _ = _bnhd(K)
     V, _ = _bnhd(V)
@@ -229,9 +251,16 @@ def quantize(Q, K, V, perm=None, vsmooth: int = 1, rope=None, hadamard: int = 0)
         perm = np.ascontiguousarray(perm, dtype=np.int32)
         p = perm.ctypes.data_as(ctypes.c_void_p)
     r, rp = _rope_table(rope, N, d)
-    rc = lib().vco_quantize_ex(Q, K, V, B, H, N, d, sb, sn, sh, p, int(vsmooth), rp, int(hadamard),
-                               out["Q8"], out["sq"], out["K8"], out["sk"], out["V8T"], out["sv"],
-                               out["mu"].ctypes.data_as(ctypes.c_void_p))
+    if vbits == 4:
+        assert rope is None and not hadamard
+        rc = lib().vco_quantize_v4(Q, K, V, B, H, N, d, sb, sn, sh, p, int(vsmooth),
+                                   out["Q8"], out["sq"], out["K8"], out["sk"], out["V8T"], out["sv"],
+                                   out["mu"].ctypes.data_as(ctypes.c_void_p))
+    else:
+        assert vbits == 8
+        rc = lib().vco_quantize_ex(Q, K, V, B, H, N, d, sb, sn, sh, p, int(vsmooth), rp, int(hadamard),
+                                   out["Q8"], out["sq"], out["K8"], out["sk"], out["V8T"], out["sv"],
+                                   out["mu"].ctypes.data_as(ctypes.c_void_p))
     assert rc == 0
     return out
 

@@ -36,6 +36,41 @@
 #define VCO_BLOCK 128 /* B_v = 128 tokens per hardware block, [R] 复现评估 / [W] */
 
 /* ------------------------------------------------------------------ */
+/* E2M1 (OCP FP4): 1 sign, 2 exponent (bias 1), 1 mantissa bit; codes  */
+/* 0-7 are 0, 0.5, 1, 1.5, 2, 3, 4, 6; no infinities or NaN.  The      */
+/* 4-bit residual of the pages' 4-bit path ([R] 方法步骤详情 ② "4 比特  */
+/* NVFP4"); its block scale is this build's reading, see               */
+/* vco_quantize_v4.                                                    */
+/* ------------------------------------------------------------------ */
+
+double vco_e2m1_decode(uint8_t c) {
+    int s = (c >> 3) & 1;
+    int e = (c >> 1) & 3;
+    int m = c & 1;
+    double v = (e == 0) ? 0.5 * (double)m : ldexp(1.0 + 0.5 * (double)m, e - 1);
+    return s ? -v : v;
+}
+
+/* Nearest code by brute force over the eight magnitudes, ties to the even
+ * code (mantissa bit 0), saturating to +-6. */
+uint8_t vco_e2m1_encode(float xf) {
+    uint8_t sign = signbit(xf) ? 8 : 0;
+    double a = fabs((double)xf);
+    if (a >= 6.0) return (uint8_t)(sign | 7);   /* saturate (distances to 4 and 6 can tie in fp64 far out) */
+    int best = 0;
+    double bd = a;
+    for (int c = 1; c < 8; ++c) {
+        double dd = fabs(a - vco_e2m1_decode((uint8_t)c));
+        if (dd < bd || (dd == bd && (c & 1) == 0)) { bd = dd; best = c; }
+    }
+    return (uint8_t)(sign | best);
+}
+
+void vco_e2m1_encode_arr(const float* x, int64_t n, uint8_t* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = vco_e2m1_encode(x[i]);
+}
+
+/* ------------------------------------------------------------------ */
 /* E4M3 (OCP FP8): 1 sign, 4 exponent (bias 7), 3 mantissa bits; no    */
 /* infinities; S.1111.111 is NaN; largest finite magnitude 448. [R]    */
 /* 前置知识 "E4M3 浮点格式".                                            */
@@ -407,12 +442,53 @@ static void quant_rows_blockscale(const uint16_t* X, int64_t s_b, int64_t s_n, i
     free(Y);
 }
 
-int vco_quantize_ex(const uint16_t* Q, const uint16_t* K, const uint16_t* V,
-                    int B, int H, int N, int d, int64_t s_b, int64_t s_n, int64_t s_h,
-                    const int32_t* perm, int vsmooth, const float* rope, int hadamard,
-                    uint8_t* Q8, float* sq, uint8_t* K8, float* sk,
-                    uint8_t* V8T, float* sv, uint16_t* mu) {
+/* 4-bit residual of one channel, read here as the OCP MX form of E2M1: the
+ * pages' 4-bit path keeps the residual in 4 bits with a per-block scale
+ * ([R] 方法步骤详情 ②, NVFP4); with FP8 probabilities on the tensor core the
+ * block-scaled kind whose A stays E4M3 takes power-of-two (UE8M0) scales per
+ * 32 elements along the product's depth -- here 32 consecutive tokens of a
+ * channel.  Steps, in fp32 where a result decides a code:
+ *   g = amax / 6 (per channel, like 448 for E4M3), x_t = fl(R_t * fl(6/amax));
+ *   per group of 32 tokens: a = max |x_t|, e = floor(log2 a) - 2 (the OCP
+ *   rule: the largest element lands in [4, 8)), clamped to [-8, 0] (e = -8
+ *   for an all-zero group);
+ *   q_t = E2M1_RNE_sat(x_t * 2^-e), value q_t 2^e.
+ * Every such value is exactly an E4M3 value (one mantissa bit, exponent
+ * >= -9), so V8T stores its E4M3 byte and sv = g: attention then computes
+ * sum_t P_t (q_t 2^e) g exactly as a block-scaled E4M3 x E2M1 product would. */
+static void v4_channel(const float* Rc, int d, int N, int64_t Npad, float amax, float* sv_c, uint8_t* row) {
+    float inv = (amax > 0.0f) ? 6.0f / amax : 0.0f;
+    *sv_c = amax / 6.0f;
+    for (int64_t t0 = 0; t0 < Npad; t0 += 32) {
+        float a = 0.0f;
+        for (int64_t t = t0; t < t0 + 32 && t < N; ++t) {
+            float x = Rc[t * d] * inv;
+            if (fabsf(x) > a) a = fabsf(x);
+        }
+        int e = -8;
+        if (a > 0.0f) {
+            int ex;
+            frexpf(a, &ex);            /* a = f 2^ex, f in [0.5, 1): floor(log2 a) = ex - 1 */
+            e = ex - 1 - 2;
+            if (e < -8) e = -8;
+            if (e > 0) e = 0;
+        }
+        for (int64_t t = t0; t < t0 + 32; ++t) {
+            if (t >= N) { row[t] = 0; continue; }
+            float x = Rc[t * d] * inv;
+            uint8_t q = vco_e2m1_encode(ldexpf(x, -e));
+            row[t] = vco_e4m3_encode((float)ldexp(vco_e2m1_decode(q), e));
+        }
+    }
+}
+
+static int quantize_impl(const uint16_t* Q, const uint16_t* K, const uint16_t* V,
+                         int B, int H, int N, int d, int64_t s_b, int64_t s_n, int64_t s_h,
+                         const int32_t* perm, int vsmooth, const float* rope, int hadamard, int vbits,
+                         uint8_t* Q8, float* sq, uint8_t* K8, float* sk,
+                         uint8_t* V8T, float* sv, uint16_t* mu) {
     if (N < 1 || d < 1 || (rope && (d & 1)) || (hadamard && (d & (d - 1)))) return 1;
+    if (vbits != 8 && vbits != 4) return 1;
     float q_mul = hadamard ? 1.0f / (float)d : 1.0f;
     int nblk = (N + VCO_BLOCK - 1) / VCO_BLOCK;
     int64_t Npad = (int64_t)nblk * VCO_BLOCK;
@@ -453,15 +529,38 @@ int vco_quantize_ex(const uint16_t* Q, const uint16_t* K, const uint16_t* V,
                 float a = fabsf(R[(int64_t)t * d + c]);
                 if (a > amax) amax = a;
             }
-            float inv = (amax > 0.0f) ? 448.0f / amax : 0.0f;
-            sv[(int64_t)bh * d + c] = amax / 448.0f;
             uint8_t* row = V8T + ((int64_t)bh * d + c) * Npad;
-            for (int64_t t = 0; t < Npad; ++t)
-                row[t] = (t < N) ? vco_e4m3_encode(R[t * d + c] * inv) : 0;
+            if (vbits == 8) {
+                float inv = (amax > 0.0f) ? 448.0f / amax : 0.0f;
+                sv[(int64_t)bh * d + c] = amax / 448.0f;
+                for (int64_t t = 0; t < Npad; ++t)
+                    row[t] = (t < N) ? vco_e4m3_encode(R[t * d + c] * inv) : 0;
+            } else {
+                v4_channel(R + c, d, N, Npad, amax, sv + (int64_t)bh * d + c, row);
+            }
         }
         free(R);
     }
     return 0;
+}
+
+int vco_quantize_ex(const uint16_t* Q, const uint16_t* K, const uint16_t* V,
+                    int B, int H, int N, int d, int64_t s_b, int64_t s_n, int64_t s_h,
+                    const int32_t* perm, int vsmooth, const float* rope, int hadamard,
+                    uint8_t* Q8, float* sq, uint8_t* K8, float* sk,
+                    uint8_t* V8T, float* sv, uint16_t* mu) {
+    return quantize_impl(Q, K, V, B, H, N, d, s_b, s_n, s_h, perm, vsmooth, rope, hadamard, 8,
+                         Q8, sq, K8, sk, V8T, sv, mu);
+}
+
+/* The quantizer with the V residual in the 4-bit form (v4_channel). */
+int vco_quantize_v4(const uint16_t* Q, const uint16_t* K, const uint16_t* V,
+                    int B, int H, int N, int d, int64_t s_b, int64_t s_n, int64_t s_h,
+                    const int32_t* perm, int vsmooth,
+                    uint8_t* Q8, float* sq, uint8_t* K8, float* sk,
+                    uint8_t* V8T, float* sv, uint16_t* mu) {
+    return quantize_impl(Q, K, V, B, H, N, d, s_b, s_n, s_h, perm, vsmooth, NULL, 0, 4,
+                         Q8, sq, K8, sk, V8T, sv, mu);
 }
 
 /* The quantizer without the rotary transform and the Hadamard rotation. */

@@ -119,6 +119,16 @@ MUTANTS = [
      "for (int c = 0; c < k; ++c)\n            if (n[c] % VCO_BLOCK) { last = c; break; }",
      "for (int c = k - 1; c >= 0; --c)\n            if (n[c] % VCO_BLOCK) { last = c; break; }",
      ["test_oracle_block_fill.py"]),
+    # 4-bit V residual (方法步骤详情 step 2, 4-bit path; the MX reading)
+    ("e2m1_ties_away", "E2M1 ties go to the odd code",
+     "if (dd < bd || (dd == bd && (c & 1) == 0))", "if (dd < bd || (dd == bd && (c & 1) == 1))",
+     ["test_oracle_v4.py"]),
+    ("e2m1_no_saturation", "E2M1 without the explicit saturation at 6",
+     "    if (a >= 6.0) return (uint8_t)(sign | 7);", "", ["test_oracle_v4.py"]),
+    ("mx_exponent_off", "MX group exponent one too high (maximum lands in [2, 4))",
+     "            e = ex - 1 - 2;", "            e = ex - 1 - 1;", ["test_oracle_v4.py"]),
+    ("v4_scale_448", "4-bit channel scale amax/448 instead of amax/6",
+     "    *sv_c = amax / 6.0f;", "    *sv_c = amax / 448.0f;", ["test_oracle_v4.py"]),
     # hybrid bytes (独立分析的弱点, weakness two)
     ("hybrid_inverted", "hybrid vote inverted",
      "if (diff >= -margin) flags", "if (diff < -margin) flags", ["test_oracle_hybrid.py"]),

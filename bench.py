@@ -32,6 +32,10 @@ fp64 reference on sampled query rows.
 bytes and the hybrid bytes (exact exponent on high-weight tiles) at several
 margins, with the attention error against an fp64 reference on sampled rows.
 
+--mode v4 compares the 8-bit and the 4-bit V residual (E2M1 with a
+power-of-two scale per 32 tokens): quantizer and attention time and the
+attention output against an fp64 reference on sampled query rows.
+
 --impl reference times the CPU oracle (the only other implementation of the
 method that exists) on a bounded sample of the same workload.
 """
@@ -58,7 +62,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--mode", default="step", choices=["step", "schedule", "sweep", "preproc", "fill", "hybrid"])
+    ap.add_argument("--mode", default="step", choices=["step", "schedule", "sweep", "preproc", "fill", "hybrid", "v4"])
     ap.add_argument("--expcast", type=int, default=1)
     ap.add_argument("--vsmooth", type=int, default=1)
     ap.add_argument("--no-e2e", action="store_true")
@@ -711,6 +715,53 @@ def run_hybrid(args):
                                  "sampled_rows": 256, "sampled_heads": heads}}), flush=True)
 
 
+def run_v4(args):
+    """8-bit against 4-bit V residual on the Wan2.2 shape: quantizer and attention
+    time (CUDA events) and O against fp64 on sampled rows, V-Smooth on."""
+    import torch
+
+    from bit_fp8_attention_means_gb300 import inputs, vc
+    dev = torch.device("cuda", 0)
+    w = inputs.WORKLOADS["wan"]
+    H = args.heads or w.H
+    Q, K, V = inputs.make_qkv(w, dev, H=H)
+    perm = vc.vc_cluster(V, w.k, w.iters)[2]
+    s = vc.shape_of(Q)
+    O = torch.empty_like(Q)
+    g = torch.Generator(device="cpu").manual_seed(7)
+    rows = torch.randperm(w.N, generator=g)[:256].to(dev)
+    heads = list(range(0, H, max(1, H // 4)))[:4]
+    ref = fp64_rows(Q, K, V, rows, heads, w.d)
+    flops = attn_flops(w.B, H, w.N, w.d)
+    out = []
+    for vbits in (8, 4):
+        qz = vc.vc_quantize(Q, K, V, perm, 1, vbits=vbits)
+
+        def timed(fn):
+            for _ in range(max(2, args.warmup)):
+                fn()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            reps = max(3, args.steps)
+            e0.record()
+            for _ in range(reps):
+                fn()
+            e1.record()
+            torch.cuda.synchronize()
+            return e0.elapsed_time(e1) / reps
+
+        q_ms = timed(lambda: vc.vc_quantize(Q, K, V, perm, 1, out=qz, vbits=vbits))
+        a_ms = timed(lambda: vc.vc_attn_fwd(qz, s, O=O))
+        err = [float((O[0, rows, h].double() - ref[h]).norm() / ref[h].norm()) for h in heads]
+        out.append({"vbits": vbits, "quantize_ms": q_ms, "attn_ms": a_ms,
+                    "attn_tflops": flops / (a_ms * 1e-3) / 1e12, "o_rel_err_vs_fp64": sum(err) / len(err),
+                    "v_bytes_4bit_packed": (w.B * H * w.d * vc.nblk_of(w.N) * 128) // 2 if vbits == 4 else None})
+    print(json.dumps({"mode": "v4", "metric": "quantizer and attention ms, O error vs fp64: 8-bit vs 4-bit V residual",
+                      "rows": out,
+                      "config": {"workload": "wan2.2-shaped B=1 H=%d N=75600 d=128, vsmooth=1, k=256 pi" % H,
+                                 "sampled_rows": 256, "sampled_heads": heads}}), flush=True)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
@@ -726,6 +777,8 @@ def main():
         run_fill(args)
     elif args.mode == "hybrid":
         run_hybrid(args)
+    elif args.mode == "v4":
+        run_v4(args)
     else:
         run_sweep(args)
 

@@ -169,6 +169,19 @@ vc_status vc_quantize_ex(const void* Q, const void* K, const void* V, vc_shape s
                            static_cast<uint16_t*>(mu), workspace, reinterpret_cast<cudaStream_t>(stream));
 }
 
+vc_status vc_quantize_v4(const void* Q, const void* K, const void* V, vc_shape shape, const int32_t* perm,
+                         int vsmooth, uint8_t* Q8, float* sq, uint8_t* K8, float* sk, uint8_t* V8T, float* sv,
+                         void* mu, void* workspace, size_t workspace_bytes, vc_stream_t stream) {
+    vc_status st = quantize_args(Q, K, V, shape, vsmooth, nullptr, 0, Q8, sq, K8, sk, V8T, sv, mu);
+    if (st != VC_OK) return st;
+    if (!workspace_ok(workspace, workspace_bytes, quantize_workspace(shape))) return VC_ERR_WORKSPACE;
+    Preproc pp;
+    pp.v4 = 1;
+    return launch_quantize(static_cast<const uint16_t*>(Q), static_cast<const uint16_t*>(K),
+                           static_cast<const uint16_t*>(V), shape, perm, vsmooth, pp, Q8, sq, K8, sk, V8T, sv,
+                           static_cast<uint16_t*>(mu), workspace, reinterpret_cast<cudaStream_t>(stream));
+}
+
 size_t vc_quantize_staged_workspace(vc_shape shape) {
     if (check_shape(shape) != VC_OK) return 0;
     return quantize_staged_workspace(shape);

@@ -45,6 +45,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_tiled_fn();
 struct Preproc {
     const float* rope = nullptr;  // [N, d/2, 2] (cos, sin), or null: no rotary transform
     int hadamard = 0;             // 1: Walsh-Hadamard transform of Q and K rows, 1/d on the Q scale
+    int v4 = 0;                   // 1: the V residual in the 4-bit form (E2M1, power-of-two scale per 32 tokens)
 };
 size_t quantize_workspace(const vc_shape& s);
 size_t quantize_staged_workspace(const vc_shape& s);

@@ -541,9 +541,20 @@ __global__ void __launch_bounds__(kVThreads) quant_v_stats_kernel(VArgs a) {
     }
 }
 
+// E2M1 value nearest to |y| <= 8 (0, 0.5, 1, 1.5, 2, 3, 4, 6), ties to the
+// even code (the one whose mantissa bit is 0), saturating at 6.
+__device__ __forceinline__ float e2m1_rne_abs(float y) {
+    return y <= 0.25f ? 0.f : y < 0.75f ? 0.5f : y <= 1.25f ? 1.f : y < 1.75f ? 1.5f
+         : y <= 2.5f ? 2.f : y < 3.5f ? 3.f : y <= 5.f ? 4.f : 6.f;
+}
+
 // Residual codes, written token-contiguous per channel (V8T [B,H,D,Npad]).
 // Thread (c, part) converts the block's tokens [part*T, part*T + T) of channel c.
-template <int D>
+// V4: the residual in the 4-bit form -- E2M1 with a power-of-two scale per 32
+// tokens of a channel (the OCP MX rule: the group's largest |x| lands in
+// [4, 8), exponent clamped to [-8, 0]) under the channel scale amax/6 -- each
+// value stored as its (equal) E4M3 byte.
+template <int D, bool V4>
 __global__ void __launch_bounds__(kVThreads) quant_v_codes_kernel(VArgs a) {
     __shared__ __align__(16) uint16_t vs[kBlock * D];
     __shared__ int32_t src_s[kBlock];
@@ -555,10 +566,47 @@ __global__ void __launch_bounds__(kVThreads) quant_v_codes_kernel(VArgs a) {
     const int c = threadIdx.x % D, part = threadIdx.x / D;
     const float m = a.vsmooth ? bf16_bits_to_f32(a.mu[((int64_t)bh * a.nblk + j) * D + c]) : 0.f;
     const float amax = __uint_as_float(a.amax_ws[(int64_t)bh * D + c]);
-    const float inv = amax > 0.f ? __fdiv_rn(448.f, amax) : 0.f;
-    if (j == 0 && part == 0) a.sv[(int64_t)bh * D + c] = __fdiv_rn(amax, 448.f);
+    constexpr float QMAX = V4 ? 6.f : 448.f;
+    const float inv = amax > 0.f ? __fdiv_rn(QMAX, amax) : 0.f;
+    if (j == 0 && part == 0) a.sv[(int64_t)bh * D + c] = __fdiv_rn(amax, QMAX);
     uint4* out =
         reinterpret_cast<uint4*>(a.V8T + ((int64_t)bh * D + c) * a.Npad + (int64_t)j * kBlock + part * T);
+    if constexpr (V4) {
+#pragma unroll
+        for (int grp = 0; grp < T / 32; ++grp) {
+            const int i0 = part * T + grp * 32;
+            float x[32];
+            float gmax = 0.f;
+#pragma unroll
+            for (int u = 0; u < 32; ++u) {
+                x[u] = (i0 + u < cnt) ? __fmul_rn(__fsub_rn(bf16_bits_to_f32(vs[(i0 + u) * D + c]), m), inv) : 0.f;
+                gmax = fmaxf(gmax, fabsf(x[u]));
+            }
+            int e = -8;
+            if (gmax > 0.f) {
+                int ex;
+                frexpf(gmax, &ex);  // gmax = f 2^ex, f in [0.5, 1): floor(log2 gmax) = ex - 1
+                e = min(max(ex - 3, -8), 0);
+            }
+            const float up = __int_as_float((127 - e) << 23), down = __int_as_float((127 + e) << 23);  // 2^-e, 2^e
+#pragma unroll
+            for (int g = 0; g < 2; ++g) {
+                uint32_t w[4];
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    float v[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const float xv = x[g * 16 + q4 * 4 + u];
+                        v[u] = copysignf(__fmul_rn(e2m1_rne_abs(fabsf(__fmul_rn(xv, up))), down), xv);
+                    }
+                    w[q4] = cvt_e4m3x2(v[0], v[1]) | (cvt_e4m3x2(v[2], v[3]) << 16);
+                }
+                out[grp * 2 + g] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+        }
+        return;
+    }
 #pragma unroll
     for (int g = 0; g < T / 16; ++g) {
         uint32_t w[4];
@@ -696,7 +744,7 @@ static cudaError_t launch_qk_pre(const QkArgs& qa, const QkArgs& ka, const vc_sh
 template <int D>
 static vc_status launch_v(const uint16_t* V, int64_t s_b, int64_t s_n, int64_t s_h, const vc_shape& s,
                           const int32_t* perm, int vsmooth, uint8_t* V8T, float* sv, uint16_t* mu, void* ws,
-                          cudaStream_t st) {
+                          cudaStream_t st, bool v4 = false) {
     const int nblk = nblk_of(s.N);
     uint32_t* amax_ws = static_cast<uint32_t*>(ws);
     cudaError_t e = cudaMemsetAsync(amax_ws, 0, quantize_workspace(s), st);
@@ -705,7 +753,8 @@ static vc_status launch_v(const uint16_t* V, int64_t s_b, int64_t s_n, int64_t s
     quant_v_stats_kernel<D><<<dim3(nblk, s.H, s.B), kVThreads, 0, st>>>(va);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_status(e);
-    quant_v_codes_kernel<D><<<dim3(nblk, s.H, s.B), kVThreads, 0, st>>>(va);
+    if (v4) quant_v_codes_kernel<D, true><<<dim3(nblk, s.H, s.B), kVThreads, 0, st>>>(va);
+    else quant_v_codes_kernel<D, false><<<dim3(nblk, s.H, s.B), kVThreads, 0, st>>>(va);
     return cuda_status(cudaGetLastError());
 }
 
@@ -725,7 +774,7 @@ static vc_status launch_quantize_d(const uint16_t* Q, const uint16_t* K, const u
     else
         e = pp.hadamard ? launch_qk_pre<D, false, true>(qa, ka, s, st) : launch_qk<D, uint16_t>(qa, ka, s, st);
     if (e != cudaSuccess) return cuda_status(e);
-    return launch_v<D>(V, s.s_b, s.s_n, s.s_h, s, perm, vsmooth, V8T, sv, mu, ws, st);
+    return launch_v<D>(V, s.s_b, s.s_n, s.s_h, s, perm, vsmooth, V8T, sv, mu, ws, st, pp.v4 != 0);
 }
 
 vc_status launch_quantize(const uint16_t* Q, const uint16_t* K, const uint16_t* V, const vc_shape& s,

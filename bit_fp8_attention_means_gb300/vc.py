@@ -59,6 +59,8 @@ def lib():
         L.vc_quantize_ex.restype = ctypes.c_int
         L.vc_quantize_ex.argtypes = [_vp, _vp, _vp, VcShape, _vp, ctypes.c_int, _vp, ctypes.c_int, _vp, _vp, _vp,
                                      _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
+        L.vc_quantize_v4.restype = ctypes.c_int
+        L.vc_quantize_v4.argtypes = L.vc_quantize.argtypes
         L.vc_quantize_staged_workspace.restype = ctypes.c_size_t
         L.vc_quantize_staged_workspace.argtypes = [VcShape]
         L.vc_quantize_staged.restype = ctypes.c_int
@@ -202,8 +204,10 @@ def _quantize_call(fn, name, Q, K, V, perm, vsmooth, rope, hadamard, out, worksp
     return out
 
 
-def vc_quantize(Q, K, V, perm=None, vsmooth=1, out=None, workspace=None, stream=None):
-    """Fused quantizer. Returns a dict with Q8, sq, K8, sk, V8T, sv, mu (mu is bf16 bits as int16)."""
+def vc_quantize(Q, K, V, perm=None, vsmooth=1, out=None, workspace=None, stream=None, vbits=8):
+    """Fused quantizer. Returns a dict with Q8, sq, K8, sk, V8T, sv, mu (mu is bf16 bits as int16).
+    vbits=4 calls vc_quantize_v4: the V residual in 4 bits (E2M1 with a power-of-two
+    scale per 32 tokens of a channel), stored as E4M3 bytes for vc_attn_fwd."""
     L = lib()
     s = _check_qkv(Q, K, V)
     dev = Q.device
@@ -211,11 +215,14 @@ def vc_quantize(Q, K, V, perm=None, vsmooth=1, out=None, workspace=None, stream=
         out = alloc_quantized(s, dev, vsmooth)
     if workspace is None:
         workspace = _workspace(L.vc_quantize_workspace(s), dev)
-    rc = L.vc_quantize(_ptr(Q), _ptr(K), _ptr(V), s, _ptr(perm), int(vsmooth), _ptr(out["Q8"]),
-                       _ptr(out["sq"]), _ptr(out["K8"]), _ptr(out["sk"]), _ptr(out["V8T"]), _ptr(out["sv"]),
-                       _ptr(out["mu"]) if vsmooth else None, _ptr(workspace), workspace.numel(),
-                       _stream(stream))
-    _check(rc, "vc_quantize")
+    if vbits not in (4, 8):
+        raise ValueError("vbits must be 4 or 8")
+    fn, name = (L.vc_quantize_v4, "vc_quantize_v4") if vbits == 4 else (L.vc_quantize, "vc_quantize")
+    rc = fn(_ptr(Q), _ptr(K), _ptr(V), s, _ptr(perm), int(vsmooth), _ptr(out["Q8"]),
+            _ptr(out["sq"]), _ptr(out["K8"]), _ptr(out["sk"]), _ptr(out["V8T"]), _ptr(out["sv"]),
+            _ptr(out["mu"]) if vsmooth else None, _ptr(workspace), workspace.numel(),
+            _stream(stream))
+    _check(rc, name)
     return out
 
 

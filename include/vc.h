@@ -237,6 +237,32 @@ vc_status vc_quantize_staged(const void* Q, const void* K, const void* V, vc_sha
                              void* workspace, size_t workspace_bytes, vc_stream_t stream);
 
 /*
+ * vc_quantize with the V residual in 4 bits: the pages' 4-bit path keeps the
+ * residual R = V' - mu_j in 4 bits with a per-block scale (paper summary
+ * 方法步骤详情 step 2, "4 比特 NVFP4"; the summary's own analysis, weakness
+ * three, and the wire.sakhanda.co section "ExpCast-FP8" note that the
+ * probabilities must stay FP8 beside it).  This library's form of it, for FP8
+ * probabilities on the tensor core: E2M1 codes with a power-of-two scale per
+ * 32 consecutive tokens of a channel (the OCP MX rule), under a per-channel
+ * fp32 scale; per (b, h, channel c):
+ *   g_c = amax_t |R[t,c]| / 6 (sv),  x_t = fl(R[t,c] * fl(6 / amax));
+ *   per group of 32 tokens (t = 32 i .. 32 i + 31): e = floor(log2 max |x_t|) - 2
+ *   clamped to [-8, 0] (-8 for an all-zero group);
+ *   q_t = E2M1_RNE_sat(x_t * 2^-e) (0, 0.5, 1, 1.5, 2, 3, 4, 6; ties to the
+ *   even code), value q_t * 2^e.
+ * Every such value is an E4M3 value, so V8T holds its E4M3 byte and
+ * vc_attn_fwd runs unchanged: the FP8 product computes exactly what a
+ * block-scaled E4M3 x E2M1 product computes, at the same tensor-core rate.
+ * Q, K and the block means are as in vc_quantize; same arguments, workspace
+ * and errors.
+ */
+vc_status vc_quantize_v4(const void* Q, const void* K, const void* V, vc_shape shape,
+                         const int32_t* perm, int vsmooth,
+                         uint8_t* Q8, float* sq, uint8_t* K8, float* sk,
+                         uint8_t* V8T, float* sv, void* mu,
+                         void* workspace, size_t workspace_bytes, vc_stream_t stream);
+
+/*
  * vc_quantize without a workspace argument, for callers that cannot allocate
  * device memory: a host that embeds this library inside a framework whose
  * memory pool owns all device memory, or code running where an allocation

@@ -91,6 +91,11 @@ def test_quantize_and_cluster_argument_errors(L):
     assert L.vc_quantize(*f, s, None, 1, *outs[:6], None, FAKE, ws_need, None) == 1   # mu needed
     ws_odd = ctypes.c_void_p(0x10000 + 128)   # workspace must be 256-byte aligned
     assert L.vc_quantize(*f, s, None, 1, *outs, ws_odd, ws_need, None) == 3
+    # the 4-bit residual entry point checks the same way
+    assert L.vc_quantize_v4(*f, s, None, 1, *outs, FAKE, ws_need - 1, None) == 3
+    assert L.vc_quantize_v4(*f, s, None, 2, *outs, FAKE, ws_need, None) == 1
+    assert L.vc_quantize_v4(*f, s, None, 1, *outs[:6], None, FAKE, ws_need, None) == 1
+    assert L.vc_quantize_v4(*f, _shape(d=96), None, 1, *outs, FAKE, ws_need, None) == 2
     cw = L.vc_cluster_workspace(s, 8)
     assert L.vc_cluster(FAKE, s, 0, 1, 0, FAKE, FAKE, FAKE, FAKE, cw, None, None) == 2
     assert L.vc_cluster(FAKE, s, 2000, 1, 0, FAKE, FAKE, FAKE, FAKE, cw, None, None) == 2

@@ -56,6 +56,9 @@ def lib():
         L.vco_e4m3_decode_arr.argtypes = [_u8p, _i64, _f64p]
         L.vco_bf16_rne_arr.argtypes = [_f32p, _i64, _u16p]
         L.vco_expcast_arr.argtypes = [_f32p, _i64, ctypes.c_float, ctypes.c_float, _u8p]
+        L.vco_expcast_piece_arr.argtypes = [_f32p, _i64, ctypes.c_float, ctypes.c_float, _u8p]
+        L.vco_expcast_C0.restype = ctypes.c_float
+        L.vco_expcast_C0.argtypes = [ctypes.c_float]
         L.vco_kmeans.restype = _int
         L.vco_kmeans.argtypes = [_u16p, _int, _int, _int, _int, _i64, _i64, _i64,
                                  _int, _int, _int, _f32p, _i32p]
@@ -152,6 +155,18 @@ def kscale_of(softmax_scale: float, d: int) -> np.float32:
 
 def expcast_C(m_new: float) -> np.float32:
     return np.float32(lib().vco_expcast_C(float(m_new)))
+
+
+def expcast_C0(m_new: float) -> np.float32:
+    return np.float32(lib().vco_expcast_C0(float(m_new)))
+
+
+def expcast_piece_codes(acc, sigma8: float, C0: float) -> np.ndarray:
+    """Range-adaptive ExpCast bytes (expcast = 3) for fp32 scores acc."""
+    a = np.ascontiguousarray(acc, dtype=np.float32).ravel()
+    out = np.empty(a.size, np.uint8)
+    lib().vco_expcast_piece_arr(a, a.size, float(sigma8), float(C0), out)
+    return out.reshape(np.shape(acc))
 
 
 def expcast_codes(acc, sigma8: float, C: float) -> np.ndarray:
@@ -272,7 +287,8 @@ def attn(qz: dict, N: int, softmax_scale: float = 0.0, expcast: int = 1, vsmooth
     expcast: 0 exp-then-cast, 1 ExpCast, 2 hybrid (exp-then-cast on the key
     tiles that are high-weight for a 32-row group: some row's tile maximum
     within ``margin`` (log2 units) of its running maximum; ``rows`` must then
-    hold whole groups).  Returns O fp64 [B,H,nrows,d] (and codes uint8
+    hold whole groups), 3 range-adaptive ExpCast (a beta per pair of codes
+    of the octave).  Returns O fp64 [B,H,nrows,d] (and codes uint8
     [B,H,nrows,Npad] if asked).
     """
     B, H, Npad, d = qz["Q8"].shape

@@ -171,6 +171,35 @@ void vco_bf16_rne_arr(const float* x, int64_t n, uint16_t* out) {
     for (int64_t i = 0; i < n; ++i) out[i] = vco_bf16_rne(x[i]);
 }
 
+/* Range-adaptive ExpCast byte (expcast = 3).  The paper summary's own
+ * analysis (独立分析的弱点, weakness two) suggests choosing beta by score
+ * range.  Reading: the range is the position of the score inside its octave
+ * of codes, in four pieces of two codes each, read off the byte ExpCast would
+ * give without beta:
+ *   t0 = fmaf(acc, 8 sigma, C0),  C0 = fmaf(-8, m', 120)
+ *   p  = (rint(t0) >> 1) & 3,     c = clip(rint(fl(t0 + beta_p)), 0, 120)
+ * beta_p maximises the agreement with the exp-then-cast byte over an octave
+ * (oracle/derive_beta_pieces.py; 94.6 % against 79.6 % for the single
+ * beta = -0.35).  A score whose t0 is negative gives 0 whatever its piece. */
+static const float VCO_BETA_PIECE[4] = {-0.195f, -0.635f, -0.685f, -0.535f};
+
+float vco_expcast_C0(float m_new) { return fmaf(-8.0f, m_new, 120.0f); }
+
+uint8_t vco_expcast_piece_code(float acc, float sigma8, float C0) {
+    float t0 = fmaf(acc, sigma8, C0);
+    if (!(t0 >= 0.0f)) return 0;              /* negatives, -inf, NaN */
+    if (t0 > 121.0f) return 120;              /* every piece clips to 120 past 120.685 */
+    long k = (long)nearbyintf(t0);            /* RNE */
+    float t1 = t0 + VCO_BETA_PIECE[(k >> 1) & 3];
+    float r1 = nearbyintf(t1);
+    if (!(r1 > 0.0f)) return 0;
+    return (uint8_t)(r1 > 120.0f ? 120.0f : r1);
+}
+
+void vco_expcast_piece_arr(const float* acc, int64_t n, float sigma8, float C0, uint8_t* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = vco_expcast_piece_code(acc[i], sigma8, C0);
+}
+
 void vco_expcast_arr(const float* acc, int64_t n, float sigma8, float C, uint8_t* out) {
     for (int64_t i = 0; i < n; ++i) out[i] = vco_expcast_code(acc[i], sigma8, C);
 }
@@ -655,7 +684,7 @@ int vco_attn_ex(const uint8_t* Q8, const float* sq, const uint8_t* K8, const flo
                 int B, int H, int N, int d, float kscale, int expcast, float margin, int vsmooth,
                 const int32_t* rows, int nrows, const float* acc_in,
                 double* O /* [B,H,nrows,d] */, uint8_t* P_out /* [B,H,nrows,Npad] or NULL */) {
-    if (N < 1 || d < 1 || expcast < 0 || expcast > 2) return 1;
+    if (N < 1 || d < 1 || expcast < 0 || expcast > 3) return 1;
     int nblk = (N + VCO_BLOCK - 1) / VCO_BLOCK;
     int64_t Npad = (int64_t)nblk * VCO_BLOCK;
     double dec[256];
@@ -703,7 +732,11 @@ int vco_attn_ex(const uint8_t* Q8, const float* sq, const uint8_t* K8, const flo
                 float mnew = fmaxf(m, sigma * mx);
                 double alpha = (m == -INFINITY) ? 0.0 : exp2((double)m - (double)mnew);
                 double r = 0.0;
-                if (expcast == 1 || (expcast == 2 && !flags[(int64_t)(i / 32) * nblk + j])) {
+                if (expcast == 3) {
+                    float C0 = vco_expcast_C0(mnew);
+                    float sig8 = 8.0f * sigma;
+                    for (int kk = 0; kk < cnt; ++kk) code[kk] = vco_expcast_piece_code(accv[kk], sig8, C0);
+                } else if (expcast == 1 || (expcast == 2 && !flags[(int64_t)(i / 32) * nblk + j])) {
                     float C = vco_expcast_C(mnew);
                     float sig8 = 8.0f * sigma;
                     for (int kk = 0; kk < cnt; ++kk) code[kk] = vco_expcast_code(accv[kk], sig8, C);

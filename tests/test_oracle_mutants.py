@@ -129,6 +129,15 @@ MUTANTS = [
      "            e = ex - 1 - 2;", "            e = ex - 1 - 1;", ["test_oracle_v4.py"]),
     ("v4_scale_448", "4-bit channel scale amax/448 instead of amax/6",
      "    *sv_c = amax / 6.0f;", "    *sv_c = amax / 448.0f;", ["test_oracle_v4.py"]),
+    # range-adaptive ExpCast (独立分析的弱点, weakness two: beta by score range)
+    ("piece_from_floor", "piece read off floor(t0) instead of rint(t0)",
+     "long k = (long)nearbyintf(t0);            /* RNE */", "long k = (long)floorf(t0);",
+     ["test_oracle_expcast_pieces.py"]),
+    ("piece_table_reversed", "beta table in reverse piece order",
+     "{-0.195f, -0.635f, -0.685f, -0.535f}", "{-0.535f, -0.685f, -0.635f, -0.195f}",
+     ["test_oracle_expcast_pieces.py"]),
+    ("piece_width_four", "pieces four codes wide instead of two",
+     "VCO_BETA_PIECE[(k >> 1) & 3]", "VCO_BETA_PIECE[(k >> 2) & 3]", ["test_oracle_expcast_pieces.py"]),
     # hybrid bytes (独立分析的弱点, weakness two)
     ("hybrid_inverted", "hybrid vote inverted",
      "if (diff >= -margin) flags", "if (diff < -margin) flags", ["test_oracle_hybrid.py"]),

@@ -28,8 +28,9 @@ labels) with the block-fill permutation (vc_cluster_ex): grouping time, the
 relative error of the dequantized V', and the attention output against an
 fp64 reference on sampled query rows.
 
---mode hybrid times the attention kernel with ExpCast bytes, exp-then-cast
-bytes and the hybrid bytes (exact exponent on high-weight tiles) at several
+--mode hybrid times the attention kernel with ExpCast bytes, range-adaptive
+ExpCast bytes (a beta per pair of codes of the octave), exp-then-cast bytes
+and the hybrid bytes (exact exponent on high-weight tiles) at several
 margins, with the attention error against an fp64 reference on sampled rows.
 
 --mode v4 compares the 8-bit and the 4-bit V residual (E2M1 with a
@@ -671,7 +672,7 @@ def fp64_rows(Q, K, V, rows, heads, d):
 
 
 def run_hybrid(args):
-    """Attention with ExpCast / exp-then-cast / hybrid bytes on the Wan2.2 shape:
+    """Attention with ExpCast / adaptive-beta / exp-then-cast / hybrid bytes on the Wan2.2 shape:
     kernel time and error against fp64 on sampled rows."""
     import torch
 
@@ -689,7 +690,7 @@ def run_hybrid(args):
     heads = list(range(0, H, max(1, H // 4)))[:4]
     ref = fp64_rows(Q, K, V, rows, heads, w.d)
     flops = attn_flops(w.B, H, w.N, w.d)
-    arms = [("expcast", dict(expcast=1)), ("hybrid_m1", dict(exact_margin=1.0)),
+    arms = [("expcast", dict(expcast=1)), ("adaptive_beta", dict(expcast=3)), ("hybrid_m1", dict(exact_margin=1.0)),
             ("hybrid_m2", dict(exact_margin=2.0)), ("hybrid_m3", dict(exact_margin=3.0)),
             ("hybrid_m5", dict(exact_margin=5.0)), ("exp_then_cast", dict(expcast=0))]
     out = []

@@ -207,7 +207,7 @@ static vc_status attn_common(const uint8_t* Q8, const float* sq, const uint8_t* 
                              int expcast, int vsmooth, void* O) {
     vc_status st = check_shape(shape);
     if (st != VC_OK) return st;
-    if ((expcast < 0 || expcast > 2) || (vsmooth != 0 && vsmooth != 1)) return VC_ERR_INVALID_ARG;
+    if ((expcast < 0 || expcast > 3) || (vsmooth != 0 && vsmooth != 1)) return VC_ERR_INVALID_ARG;
     if (!Q8 || !sq || !K8 || !sk || !V8T || !sv || !O || (vsmooth && !mu)) return VC_ERR_INVALID_ARG;
     if (!aligned16(Q8) || !aligned16(K8) || !aligned16(V8T) || !aligned16(O)) return VC_ERR_INVALID_ARG;
     return VC_OK;
@@ -216,7 +216,7 @@ static vc_status attn_common(const uint8_t* Q8, const float* sq, const uint8_t* 
 vc_status vc_attn_fwd(const uint8_t* Q8, const float* sq, const uint8_t* K8, const float* sk, const uint8_t* V8T,
                       const float* sv, const void* mu, vc_shape shape, float softmax_scale, int expcast, int vsmooth,
                       void* O, int32_t* dev_status, vc_stream_t stream) {
-    if (expcast != 0 && expcast != 1) return VC_ERR_INVALID_ARG;
+    if (expcast == 2) return VC_ERR_INVALID_ARG;  // the hybrid has its own entry point
     vc_status st = attn_common(Q8, sq, K8, sk, V8T, sv, mu, shape, expcast, vsmooth, O);
     if (st != VC_OK) return st;
     return launch_attn(Q8, sq, K8, sk, V8T, sv, static_cast<const uint16_t*>(mu), shape, softmax_scale, expcast, 0.f,

@@ -175,6 +175,47 @@ __device__ __forceinline__ uint32_t expcast4(const float* a, float k1, float k2)
     return prmt(prmt(u0, u1, 0x0040u), prmt(u2, u3, 0x0040u), 0x5410u);
 }
 
+// Range-adaptive ExpCast (expcast = 3): beta chosen by which pair of codes of
+// its octave rint(t0) falls on, t0 = acc 8 sigma + 120 - 8 m' (ExpCast's t
+// without beta); each beta maximises agreement with the exp-then-cast byte
+// over its piece.
+constexpr float kBetaPiece0 = -0.195f, kBetaPiece1 = -0.635f, kBetaPiece2 = -0.685f, kBetaPiece3 = -0.535f;
+
+// u: bits of rint(t0) + 1.5 * 2^23, so bits 1-2 hold the piece.
+__device__ __forceinline__ float piece_beta(uint32_t u) {
+    const float lo = (u & 2u) ? kBetaPiece1 : kBetaPiece0;
+    const float hi = (u & 2u) ? kBetaPiece3 : kBetaPiece2;
+    return (u & 4u) ? hi : lo;
+}
+
+// Four range-adaptive bytes, packed little-endian.  ts = sat(acc k1 + k2) is
+// t0/128 clipped to [0, 1]; ts*128 + magic gives rint(t0) (the piece), then
+// fl(ts*128 + beta) + magic gives rint(t0 + beta) in the low byte.  With
+// t0 >= 0, t0 + beta > -0.5, so the byte never wraps below zero.
+template <bool CLIP>
+__device__ __forceinline__ uint32_t expcast4_pieces(const float* a, float k1, float k2) {
+    const float t0 = fma_sat(a[0], k1, k2);
+    const float t1 = fma_sat(a[1], k1, k2);
+    const float t2 = fma_sat(a[2], k1, k2);
+    const float t3 = fma_sat(a[3], k1, k2);
+    const float2 mg = make_float2(kMagic, kMagic), c128 = make_float2(128.f, 128.f), one = make_float2(1.f, 1.f);
+    const float2 k01 = __ffma2_rn(make_float2(t0, t1), c128, mg);
+    const float2 k23 = __ffma2_rn(make_float2(t2, t3), c128, mg);
+    const float2 b01 = make_float2(piece_beta(__float_as_uint(k01.x)), piece_beta(__float_as_uint(k01.y)));
+    const float2 b23 = make_float2(piece_beta(__float_as_uint(k23.x)), piece_beta(__float_as_uint(k23.y)));
+    const float2 r01 = __ffma2_rn(__ffma2_rn(make_float2(t0, t1), c128, b01), one, mg);
+    const float2 r23 = __ffma2_rn(__ffma2_rn(make_float2(t2, t3), c128, b23), one, mg);
+    uint32_t u0 = __float_as_uint(r01.x), u1 = __float_as_uint(r01.y);
+    uint32_t u2 = __float_as_uint(r23.x), u3 = __float_as_uint(r23.y);
+    if (CLIP) {
+        u0 = min(u0 & 0xFFu, 120u);
+        u1 = min(u1 & 0xFFu, 120u);
+        u2 = min(u2 & 0xFFu, 120u);
+        u3 = min(u3 & 0xFFu, 120u);
+    }
+    return prmt(prmt(u0, u1, 0x0040u), prmt(u2, u3, 0x0040u), 0x5410u);
+}
+
 __device__ __forceinline__ uint16_t bf16_rn_bits(float x) { return __bfloat16_as_ushort(__float2bfloat16_rn(x)); }
 
 // This thread's 64 scores of half `hf` of the key tile, from TMEM.
@@ -216,7 +257,8 @@ __device__ __forceinline__ float max64(const float (&a)[64]) {
 }
 
 // EC: 0 exp-then-cast, 1 ExpCast, 2 hybrid (exp-then-cast on the key tiles
-// that are high-weight for the warp's 32 query rows, ExpCast elsewhere).
+// that are high-weight for the warp's 32 query rows, ExpCast elsewhere),
+// 3 range-adaptive ExpCast (a beta per pair of codes of the octave).
 template <int D, int EC, bool VSMOOTH, bool DBG>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -593,11 +635,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             if constexpr (EC == 2)
                 exact_tile = __any_sync(0xffffffffu, qrow < p.N && __fsub_rn(smx, m_new) >= -p.exact_margin);
             const float alpha = ex2_approx(m - m_new);
-            const float Cc = __fmaf_rn(-8.f, m_new, 119.65f);
+            const float Cc = __fmaf_rn(-8.f, m_new, EC == 3 ? 120.f : 119.65f);
             const float k1 = sigma * 0.0625f;
             const float k2 = Cc * 0.0078125f;
             const float off = __fsub_rn(8.f, m_new);
             // |m'| < 2^19 in every row of the warp: the clip at 120 is implied
+            // (t stays below 120.5 + beta for ExpCast, below 120.5 for the
+            // adaptive t0, whose piece at 120 then carries beta = -0.195)
             const bool fast = __all_sync(0xffffffffu, fabsf(m_new) < 524288.f);
             // second read: probability bytes, half by half, into columns [32, 64)
             // of S_X, whose scores (keys 32..63) were read by then
@@ -611,7 +655,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (hf * 64 + i >= tail) a[i] = -INFINITY;
                 }
                 uint32_t pw[16];
-                if (!exact_tile) {
+                if constexpr (EC == 3) {
+                    if (fast) {
+#pragma unroll
+                        for (int w = 0; w < 16; ++w) pw[w] = expcast4_pieces<false>(a + 4 * w, k1, k2);
+                    } else {
+#pragma unroll
+                        for (int w = 0; w < 16; ++w) pw[w] = expcast4_pieces<true>(a + 4 * w, k1, k2);
+                    }
+                } else if (!exact_tile) {
                     if (fast) {
 #pragma unroll
                         for (int w = 0; w < 16; ++w) pw[w] = expcast4<false>(a + 4 * w, k1, k2);
@@ -791,6 +843,7 @@ vc_status launch_g(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorM
                    dim3 grid, cudaStream_t st, int expcast, int vsmooth) {
     if (expcast == 1) return launch_e<D, 1, G>(mq, mk, mv, p, grid, st, vsmooth);
     if (expcast == 2) return launch_e<D, 2, G>(mq, mk, mv, p, grid, st, vsmooth);
+    if (expcast == 3) return launch_e<D, 3, G>(mq, mk, mv, p, grid, st, vsmooth);
     return launch_e<D, 0, G>(mq, mk, mv, p, grid, st, vsmooth);
 }
 

@@ -254,6 +254,8 @@ def vc_attn_fwd(qz, shape: VcShape, softmax_scale=0.0, expcast=1, vsmooth=1, O=N
     exact_margin (float) selects the hybrid bytes (vc_attn_fwd_hybrid):
     exp-then-cast on the key tiles within that many log2 units of a row's
     running maximum, ExpCast elsewhere; expcast is then ignored.
+    expcast: 0 exp-then-cast, 1 ExpCast, 3 range-adaptive ExpCast (a beta per
+    pair of codes of the octave).
     debug=(bh, qtile) additionally returns the fp32 scores and probability bytes
     of that one query tile: (O, S_dump [128, Npad], P_dump [128, Npad]).
     """

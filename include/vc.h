@@ -302,6 +302,12 @@ vc_status vc_quantize_static(const void* Q, const void* K, const void* V, vc_sha
  *   m'     = max(m, sigma * max_k acc)
  *   expcast=1: c = clamp(rint(fmaf(acc, 8 sigma, fmaf(-8, m', 119.65f))), 0, 120)
  *   expcast=0: c = E4M3_RNE_sat(exp2(fmaf(acc, sigma, 8 - m')))
+ *   expcast=3: range-adaptive ExpCast (the paper summary's own analysis,
+ *              独立分析的弱点 weakness two: beta chosen by score range).
+ *              t0 = fmaf(acc, 8 sigma, fmaf(-8, m', 120)),
+ *              p  = (rint(t0) >> 1) & 3  (the pair of codes of its octave),
+ *              c  = clamp(rint(fl(t0 + beta_p)), 0, 120), c = 0 for t0 < 0,
+ *              beta = {-0.195, -0.635, -0.685, -0.535} (fp32 constants).
  *   r_ij   = sum_k decode(c)            (row sum of the quantized P)
  *   l     <- alpha l + r_ij,  alpha = exp2(m - m')
  *   A     <- alpha A + P_q V8_res * s_v + r_ij mu_j   (mu term only if vsmooth)
@@ -314,7 +320,7 @@ vc_status vc_quantize_static(const void* Q, const void* K, const void* V, vc_sha
  * (rows are written 16 bytes at a time).
  * Errors, all returned before any launch: VC_ERR_INVALID_ARG (a null pointer
  * -- mu may be NULL only with vsmooth = 0 --, a misaligned Q8, K8, V8T or O,
- * expcast or vsmooth not in {0,1}, a non-positive size, or a stride that is
+ * expcast not in {0,1,3}, vsmooth not in {0,1}, a non-positive size, or a stride that is
  * not a positive multiple of 8), VC_ERR_UNSUPPORTED (d not 64 or 128,
  * N > 2^24, or B*H*Npad >= 2^31); VC_ERR_CUDA if a tensor map cannot be
  * encoded or the launch fails.
@@ -352,8 +358,8 @@ vc_status vc_attn_fwd_hybrid(const uint8_t* Q8, const float* sq, const uint8_t* 
  * probability bytes it fed to the PV product, P_dump uint8 [128, Npad]
  * (rows = the tile's 128 query rows, columns = keys in stored order).
  * expcast = 2 runs the hybrid bytes of vc_attn_fwd_hybrid with exact_margin
- * (ignored for 0 and 1).  Same contract as vc_attn_fwd otherwise; slower (a
- * separate instantiation).
+ * (ignored for 0, 1 and 3).  Same contract as vc_attn_fwd otherwise; slower
+ * (a separate instantiation).
  */
 vc_status vc_attn_fwd_debug(const uint8_t* Q8, const float* sq, const uint8_t* K8, const float* sk,
                             const uint8_t* V8T, const float* sv, const void* mu, vc_shape shape,

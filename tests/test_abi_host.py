@@ -57,6 +57,8 @@ def test_attn_argument_errors(L):
     args = [FAKE] * 7
     assert L.vc_attn_fwd(*args, _shape(d=96), 0.0, 1, 1, FAKE, None, None) == 2
     assert L.vc_attn_fwd(*args, s, 0.0, 2, 1, FAKE, None, None) == 1
+    assert L.vc_attn_fwd(*args, s, 0.0, 4, 1, FAKE, None, None) == 1
+    assert L.vc_attn_fwd(*args, s, 0.0, -1, 1, FAKE, None, None) == 1
     assert L.vc_attn_fwd_hybrid(*args, s, 0.0, float("nan"), 1, FAKE, None, None) == 1
     assert L.vc_attn_fwd_hybrid(*args, s, 0.0, 2.0, 3, FAKE, None, None) == 1
     assert L.vc_attn_fwd_hybrid(*args, _shape(d=96), 0.0, 2.0, 1, FAKE, None, None) == 2

@@ -176,7 +176,7 @@ def _slice_bh(qz_np, b, h):
     return {k: (v[b:b + 1, h:h + 1] if v is not None else None) for k, v in qz_np.items()}
 
 
-@pytest.mark.parametrize("expcast", [1, 0])
+@pytest.mark.parametrize("expcast", [1, 0, 3])
 @pytest.mark.parametrize("N,d,qtile", [(1024, 64, 3), (1000, 128, 7), (300, 128, 0), (300, 128, 2)])
 def test_expcast_bytes_bitexact(oracle_mod, expcast, N, d, qtile):
     Q, K, V = _case(N=N, d=d, H=2, seed=17)
@@ -205,7 +205,7 @@ ATTN_CASES = [dict(N=1024, d=64, H=2, k=8), dict(N=1000, d=128, H=2, k=16), dict
 
 
 @pytest.mark.parametrize("case", ATTN_CASES, ids=lambda c: "N%d_d%d" % (c["N"], c["d"]))
-@pytest.mark.parametrize("expcast,vsmooth", [(1, 1), (1, 0), (0, 1), (0, 0)])
+@pytest.mark.parametrize("expcast,vsmooth", [(1, 1), (1, 0), (0, 1), (0, 0), (3, 1), (3, 0)])
 def test_attention_matches_oracle(oracle_mod, case, expcast, vsmooth):
     Q, K, V = _case(N=case["N"], d=case["d"], H=case["H"], seed=19)
     N = case["N"]
@@ -216,11 +216,11 @@ def test_attention_matches_oracle(oracle_mod, case, expcast, vsmooth):
     ref = oracle_mod.attn(qn, N, expcast=expcast, vsmooth=vsmooth)
     got = O.float().cpu().numpy().transpose(0, 2, 1, 3)
     oracle_mod.check_o(got, ref, "N%d d%d expcast %d vsmooth %d" % (N, case["d"], expcast, vsmooth),
-                        exp_bytes=expcast != 1)
+                        exp_bytes=expcast == 0)
 
 
 @pytest.mark.parametrize("d", [64, 128])
-@pytest.mark.parametrize("expcast", [1, 0])
+@pytest.mark.parametrize("expcast", [1, 0, 3])
 def test_attention_batched_with_scale(oracle_mod, d, expcast):
     """B = 2 and a softmax scale other than 1/sqrt(d): every (b, h) against the oracle."""
     N, scale = 700, 0.05
@@ -234,7 +234,7 @@ def test_attention_batched_with_scale(oracle_mod, d, expcast):
     got = O.float().cpu().numpy().transpose(0, 2, 1, 3)
     for b in range(2):
         for h in range(2):
-            oracle_mod.check_o(got[b, h], ref[b, h], "b%d h%d" % (b, h), exp_bytes=expcast != 1)
+            oracle_mod.check_o(got[b, h], ref[b, h], "b%d h%d" % (b, h), exp_bytes=expcast == 0)
 
 
 def test_output_rows_beyond_n_untouched(oracle_mod):

@@ -67,6 +67,8 @@ def parse():
     ap.add_argument("--expcast", type=int, default=1)
     ap.add_argument("--vsmooth", type=int, default=1)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-numa-bind", action="store_true",
+                    help="allocate the pinned e2e buffers without binding to the GPU's NUMA node")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--heads", type=int, default=0,
                     help="profiling aid: run the workload with this many heads instead of its own")
@@ -349,6 +351,51 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def _cpulist(text):
+    cpus = set()
+    for part in text.strip().split(","):
+        if not part:
+            continue
+        lo, _, hi = part.partition("-")
+        cpus.update(range(int(lo), int(hi or lo) + 1))
+    return cpus
+
+
+def gpu_host_node(dev_index):
+    """NUMA node of the host CPUs attached to the GPU (sysfs, via its PCI address),
+    or None.  On Grace machines the GPU's own memory shows up as further nodes
+    without CPUs; only a node with CPUs is returned."""
+    import torch
+    props = torch.cuda.get_device_properties(dev_index)
+    try:
+        addr = "%04x:%02x:%02x.0" % (props.pci_domain_id, props.pci_bus_id, props.pci_device_id)
+        with open("/sys/bus/pci/devices/%s/numa_node" % addr) as f:
+            node = int(f.read())
+        with open("/sys/devices/system/node/node%d/cpulist" % node) as f:
+            cpus = _cpulist(f.read())
+    except (AttributeError, OSError, ValueError):
+        return None, set()
+    return (node, cpus) if node >= 0 and cpus else (None, set())
+
+
+def pinned_pages_nodes(ptr):
+    """Host NUMA nodes holding the pages of the mapping that contains ptr, from
+    /proc/self/numa_maps ({node: pages}), or None if the kernel does not say."""
+    try:
+        with open("/proc/self/maps") as f:
+            start = next(int(a, 16) for a, b in (ln.split()[0].split("-") for ln in f)
+                         if int(a, 16) <= ptr < int(b, 16))
+        with open("/proc/self/numa_maps") as f:
+            for ln in f:
+                fields = ln.split()
+                if int(fields[0], 16) == start:
+                    out = {int(k[1:]): int(v) for k, v in (x.split("=") for x in fields if x[:1] == "N" and "=" in x)}
+                    return out or None
+    except (OSError, StopIteration, ValueError):
+        return None
+    return None
+
+
 def e2e_run(args, Q, K, V, run_on):
     """Same metric through the public API with host buffers, pipelined the way a
     serving loop would run it: every step copies its Q/K/V from pinned host
@@ -359,8 +406,21 @@ def e2e_run(args, Q, K, V, run_on):
     the current stream and returns its O."""
     import torch
     n_steps = max(2, args.steps)
-    hQ, hK, hV = (t.cpu().pin_memory() for t in (Q, K, V))
-    hO = [torch.empty(Q.shape, dtype=Q.dtype).pin_memory() for _ in range(2)]
+    # pinned buffers on the host memory next to the GPU: allocate them from the
+    # CPUs of the GPU's NUMA node (first touch places the pages there)
+    node, cpus = gpu_host_node(Q.device.index or 0)
+    allowed = os.sched_getaffinity(0)
+    bound = bool(cpus & allowed) and not args.no_numa_bind
+    if bound:
+        os.sched_setaffinity(0, cpus & allowed)
+    try:
+        hQ, hK, hV = (t.cpu().pin_memory() for t in (Q, K, V))
+        hO = [torch.empty(Q.shape, dtype=Q.dtype).pin_memory() for _ in range(2)]
+    finally:
+        if bound:
+            os.sched_setaffinity(0, allowed)
+    host_numa = {"gpu_node": node, "bound": bound, "pages_of_Q": pinned_pages_nodes(hQ.data_ptr()),
+                 "pages_of_O": pinned_pages_nodes(hO[0].data_ptr())}
     bufs = [(Q, K, V, torch.empty_like(Q)), tuple(torch.empty_like(t) for t in (Q, K, V, Q))]
     comp = torch.cuda.current_stream()
     cp = torch.cuda.Stream()     # host -> device
@@ -426,7 +486,8 @@ def e2e_run(args, Q, K, V, run_on):
             "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes, "steps": n_steps,
             "h2d_gbs": h2d_bytes / (t0.elapsed_time(t1) * 1e-3) / 1e9,
             "d2h_gbs": d2h_bytes / (t1.elapsed_time(t2) * 1e-3) / 1e9,
-            "overlap": "H2D of step i+1 and D2H of step i on two copy streams during step i"}
+            "overlap": "H2D of step i+1 and D2H of step i on two copy streams during step i",
+            "host_numa": host_numa}
 
 
 def run_reference(args):

@@ -79,3 +79,14 @@ def test_fp8_peak_burst_only_at_full_clock_without_power_cap():
     none = {"sm_mhz": None, "sm_max_mhz": None, "reasons": []}
     p = bench.fp8_peak_for(dict(peaks, sustained_sm_mhz=None), none)
     assert p["which"] == "sustained" and p["clock_matched"] is None
+
+
+def test_numa_helpers():
+    """The e2e leg binds its pinned buffers to the GPU's NUMA node: the sysfs
+    cpulist parser and the page-placement query it reports with."""
+    import numpy as np
+    assert bench._cpulist("0-3,8,10-11\n") == {0, 1, 2, 3, 8, 10, 11}
+    assert bench._cpulist("") == set()
+    buf = np.ones(1 << 22, np.uint8)          # 4 MB, touched: its pages are resident
+    nodes = bench.pinned_pages_nodes(buf.ctypes.data)
+    assert nodes is None or (sum(nodes.values()) > 0 and all(n >= 0 for n in nodes))

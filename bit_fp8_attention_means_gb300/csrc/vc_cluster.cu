@@ -5,10 +5,16 @@
 // previous denoising step's centroids, then pi = argsort(z); dimensionstp.github.io
 // section 2-1 (K' = K[pi], V' = V[pi]).
 //
-// One Lloyd iteration = four launches:
-//   centroid_norms   |c_i|^2 in fp32.
-//   assign_kernel    z_t = argmin_i |c_i|^2 - 2 v_t.c_i (fp32 CUDA-core tiles:
-//                    128 tokens x 64 centroids per step, 8x4 register blocking).
+// One Lloyd iteration = an assignment, the counting sort and the update:
+//   assign_tc_kernel (k <= 256, the case the workloads use)
+//                    z_t = argmin_i |c_i|^2 - 2 v_t.c_i with v.c on tcgen05
+//                    (bf16 token tiles by TMA against the centroids split into
+//                    two bf16 parts, fp32 accumulators in TMEM; |c|^2 and the
+//                    argmin in the epilogue warps); one persistent launch.
+//   centroid_norms + assign_kernel (k > 256)
+//                    |c_i|^2 in fp32, then the same argmin on fp32 CUDA-core
+//                    tiles (128 tokens x 64 centroids per step, 8x4 register
+//                    blocking).
 //   seg_hist / seg_scan / seg_scatter
 //                    stable counting sort of z in segments of kSeg tokens:
 //                    per-segment histograms, one exclusive scan per head in

@@ -167,8 +167,11 @@ def _pipeline(Q, K, V, k, iters, vsmooth, expcast, debug=None, use_cluster=True,
     Qd, Kd, Vd = Q.to(DEV), K.to(DEV), V.to(DEV)
     perm = vc.vc_cluster(Vd, k, iters)[2] if use_cluster else None
     qz = vc.vc_quantize(Qd, Kd, Vd, perm, vsmooth)
-    res = vc.vc_attn_fwd(qz, vc.shape_of(Qd), expcast=expcast, vsmooth=vsmooth, debug=debug, exact_margin=margin)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    res = vc.vc_attn_fwd(qz, vc.shape_of(Qd), expcast=expcast, vsmooth=vsmooth, debug=debug, exact_margin=margin,
+                         dev_status=status)
     torch.cuda.synchronize()
+    assert int(status.item()) == 0, "a device wait ran out (status %d)" % int(status.item())
     return perm, qz, res
 
 

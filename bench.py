@@ -143,7 +143,7 @@ def measured_peaks():
 
 
 def fp8_peak_for(peaks, clocks):
-    """The dense FP8 peak a tensor-bound kernel is judged against, from the
+    """The dense FP8 peak a tensor-bound kernel is compared with, from the
     measured bf16 GEMM peaks (x2, the nominal fp8/bf16 ratio).
 
     The burst figure applies when the kernel ran at full clock without the

@@ -40,13 +40,7 @@ CtxGetCurrentFn ctx_get_current_fn() {
     return fn;
 }
 
-struct AttrEntry {
-    CtxKey key;
-    const void* kern;
-    int bytes;
-};
-std::mutex g_attr_mutex;
-std::vector<AttrEntry> g_attr_done;
+CtxAttrCache g_smem_attr;
 }  // namespace
 
 vc_status current_ctx(CtxKey* out) {
@@ -64,15 +58,13 @@ vc_status ensure_smem_attr(const void* kern, int bytes) {
     CtxKey key;
     vc_status st = current_ctx(&key);
     if (st != VC_OK) return st;
-    std::lock_guard<std::mutex> lock(g_attr_mutex);
-    for (const AttrEntry& e : g_attr_done)
-        if (e.kern == kern && e.key == key && e.bytes >= bytes) return VC_OK;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    if (e != cudaSuccess) return cuda_status(e);
-    // a context created by this call's own runtime initialisation is known only now
-    if (!key.ctx) current_ctx(&key);
-    g_attr_done.push_back(AttrEntry{key, kern, bytes});
-    return VC_OK;
+    return g_smem_attr.ensure(key, kern, bytes, [&](CtxKey* k) -> vc_status {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        if (e != cudaSuccess) return cuda_status(e);
+        // a context created by this call's own runtime initialisation is known only now
+        if (!k->ctx) current_ctx(k);
+        return VC_OK;
+    });
 }
 
 vc_status quantize_args(const void* Q, const void* K, const void* V, const vc_shape& shape, int vsmooth,

@@ -5,6 +5,7 @@
 #include <cudaTypedefs.h>
 
 #include "vc.h"
+#include "vc_ctx_cache.h"
 
 namespace vc {
 
@@ -16,14 +17,8 @@ inline int64_t npad_of(int N) { return (int64_t)nblk_of(N) * kBlock; }
 vc_status check_shape(const vc_shape& s);
 vc_status cuda_status(cudaError_t e);
 
-// The CUDA context current on this host thread and its device: the key of
-// every per-device cache below (a context destroyed by a device reset and
-// recreated gets a new handle, so nothing cached for the old one is reused).
-struct CtxKey {
-    int device = -1;
-    const void* ctx = nullptr;
-    bool operator==(const CtxKey& o) const { return device == o.device && ctx == o.ctx; }
-};
+// The CUDA context current on this host thread and its device (CtxKey, in
+// vc_ctx_cache.h): the key of every per-context cache below.
 vc_status current_ctx(CtxKey* out);
 
 // Raises the dynamic shared-memory limit of kernel `kern` to `bytes` once per

@@ -52,3 +52,32 @@ def test_wan_full_size_sampled(oracle_mod):
         ref = oracle_mod.attn(want, N, rows=rows)[0, 0]
         got = O[0, rows, h].float().cpu().numpy()
         oracle_mod.check_o(got, ref, "wan head %d" % h)
+
+
+@pytest.mark.parametrize("mode", ["exp_then_cast", "hybrid_m2"])
+def test_wan_full_size_other_bytes(oracle_mod, mode):
+    """The exp-then-cast and hybrid probability bytes at the full Wan2.2 shape:
+    O on sampled rows of the last head (incl. the masked last tile) within
+    the oracle's bars for exponential-derived bytes."""
+    w = inputs.WORKLOADS["wan"]
+    Q, K, V = inputs.make_qkv(w, DEV)
+    perm = vc.vc_cluster(V, w.k, w.iters)[2]
+    qz = vc.vc_quantize(Q, K, V, perm, 1)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    if mode == "exp_then_cast":
+        O = vc.vc_attn_fwd(qz, vc.shape_of(Q), expcast=0, vsmooth=1, dev_status=status)
+        kw = dict(expcast=0)
+    else:
+        O = vc.vc_attn_fwd(qz, vc.shape_of(Q), vsmooth=1, exact_margin=2.0, dev_status=status)
+        kw = dict(expcast=2, margin=2.0)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    h = w.H - 1
+    one = {k: qz[k][:, h:h + 1].cpu().numpy() for k in ("Q8", "sq", "K8", "sk", "V8T", "sv")}
+    one["mu"] = qz["mu"][:, h:h + 1].cpu().numpy().view(np.uint16)
+    rng = np.random.default_rng(11)
+    # the hybrid votes over whole 32-row groups: sample whole groups
+    groups = np.unique(sampled_rows(w.N, rng, 6) // 32)
+    rows = np.concatenate([np.arange(g * 32, min(w.N, g * 32 + 32)) for g in groups]).astype(np.int32)
+    ref = oracle_mod.attn(one, w.N, vsmooth=1, rows=rows, **kw)[0, 0]
+    oracle_mod.check_o(O[0, rows, h].float().cpu().numpy(), ref, "wan %s head %d" % (mode, h), exp_bytes=True)
